@@ -1,0 +1,67 @@
+"""Test helpers: turn the seeded synthetic tensors into the oracle's numpy structures
+and compare results.  Shared by CPU and GPU tests; holds no arithmetic of the method."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from oracle import dit_oracle as O
+
+
+def to_np(t, dtype=np.float64):
+    if t is None:
+        return None
+    return t.detach().to("cpu", torch.float32).numpy().astype(dtype)
+
+
+def oracle_config(wd) -> O.Config:
+    return O.Config(hidden=wd.hidden, heads=wd.heads, head_dim=wd.head_dim,
+                    mlp_hidden=wd.mlp_hidden, n_dual=wd.n_dual, n_single=wd.n_single,
+                    in_channels=wd.in_channels, txt_dim=wd.txt_dim)
+
+
+def oracle_stream(w, dtype=np.float64) -> O.StreamWeights:
+    return O.StreamWeights(**{k: to_np(v, dtype) for k, v in w.items()})
+
+
+def oracle_single(w, dtype=np.float64) -> O.SingleWeights:
+    return O.SingleWeights(**{k: to_np(v, dtype) for k, v in w.items()})
+
+
+def oracle_weights(wd, w, dtype=np.float64) -> O.Weights:
+    cfg = oracle_config(wd)
+    return O.Weights(cfg=cfg, t_in=to_np(w["mod"]["t_in"], dtype), t_out=to_np(w["mod"]["t_out"], dtype),
+                     mod=to_np(w["mod"]["mod"], dtype), x_emb=to_np(w["x_emb"], dtype),
+                     ctx_emb=to_np(w["ctx_emb"], dtype), proj_out=to_np(w["proj_out"], dtype),
+                     dual=[(oracle_stream(a, dtype), oracle_stream(b, dtype)) for a, b in w["dual"]],
+                     single=[oracle_single(s, dtype) for s in w["single"]])
+
+
+def cosine(a, b) -> float:
+    a = np.asarray(a, dtype=np.float64).ravel()
+    b = np.asarray(b, dtype=np.float64).ravel()
+    return float(a @ b / (np.linalg.norm(a) * np.linalg.norm(b) + 1e-300))
+
+
+def max_abs(a, b) -> float:
+    return float(np.max(np.abs(np.asarray(a, np.float64) - np.asarray(b, np.float64))))
+
+
+def read_kv(path):
+    out = {}
+    for line in open(path):
+        line = line.split("#", 1)[0].strip()
+        if not line:
+            continue
+        k, v = [s.strip() for s in line.split("=", 1)]
+        out[k] = v
+    return out
+
+
+def read_rows(path):
+    rows = []
+    for line in open(path):
+        line = line.split("#", 1)[0].strip()
+        if line:
+            rows.append([int(x) for x in line.split()])
+    return np.asarray(rows, dtype=np.int64)

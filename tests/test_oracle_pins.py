@@ -1,0 +1,368 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+Each test is chosen so that a plausible slip in the oracle (a dropped term, a wrong
+sign, index or axis, a transposed operand, a swapped stream) fails it.  None of them
+re-types the oracle's own formula: they use golden values from the pages, closed forms,
+invariants, library routines (torch, scipy) for special cases, and brute force.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import dit_oracle as O
+from diffusion_transformer_step_gb300 import synth
+import helpers as Hx
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+STRUCT = Hx.read_kv(os.path.join(GOLD, "klein_structure.txt"))
+THETA = float(STRUCT["rope_theta"])
+AXIS = int(STRUCT["rope_dims_per_axis"])
+AXES = (AXIS,) * int(STRUCT["rope_axes"])
+RNG = np.random.default_rng(1234)
+
+
+# ------------------------------------------------------------------ token ids / RoPE
+def test_token_ids_golden_layout():
+    want = Hx.read_rows(os.path.join(GOLD, "token_ids_small.txt"))
+    got = O.token_ids(3, 2, 3, ref_grids=[(1, 2), (2, 1)])
+    np.testing.assert_array_equal(got, want)
+
+
+def test_token_ids_reference_t_offsets_and_counts():
+    n_txt = int(STRUCT["text_rows"])
+    first, step = int(STRUCT["ref_t_first"]), int(STRUCT["ref_t_step"])
+    ids = O.token_ids(n_txt, 64, 64, ref_grids=[(4, 5), (3, 3), (2, 7)])
+    assert ids.shape == (n_txt + 4096 + 20 + 9 + 14, 4)
+    ref = ids[n_txt + 4096:]
+    assert sorted(set(ref[:, 0].tolist())) == [first, first + step, first + 2 * step]
+    assert int(STRUCT["max_references"]) == 3
+    # text rows: only the sequence axis moves; image rows: l == 0 and t == 0
+    assert (ids[:n_txt, :3] == 0).all() and (ids[:n_txt, 3] == np.arange(n_txt)).all()
+    assert (ids[n_txt:n_txt + 4096, [0, 3]] == 0).all()
+
+
+def _rot(x, ids):
+    c, s = O.rope_table(np.asarray(ids, np.float64), AXES, THETA)
+    return O.apply_rope(x[None, :, None, :], c, s)[0, :, 0, :]
+
+
+def test_rope_position_zero_is_identity():
+    x = RNG.standard_normal((5, 128))
+    np.testing.assert_array_equal(_rot(x, np.zeros((5, 4))), x)
+
+
+def test_rope_preserves_every_pair_norm():
+    x = RNG.standard_normal((7, 128))
+    ids = RNG.integers(0, 5000, size=(7, 4))
+    y = _rot(x, ids)
+    n_in = np.hypot(x[:, 0::2], x[:, 1::2])
+    n_out = np.hypot(y[:, 0::2], y[:, 1::2])
+    np.testing.assert_allclose(n_out, n_in, rtol=1e-12, atol=1e-12)
+
+
+def test_rope_matches_complex_rotation_with_pages_constants():
+    # Independent route: each adjacent pair is a complex number turned by e^{i*angle},
+    # angle = pos_axis * theta^(-2j/32) with the golden theta and axis width.
+    x = RNG.standard_normal((6, 128))
+    ids = RNG.integers(0, 300, size=(6, 4)).astype(np.float64)
+    z = x[:, 0::2] + 1j * x[:, 1::2]
+    pos = np.repeat(ids, AXIS // 2, axis=1)                      # pair -> owning axis
+    jj = np.tile(np.arange(AXIS // 2), 4)
+    zr = z * np.exp(1j * pos * np.power(THETA, -2.0 * jj / AXIS))
+    want = np.empty_like(x)
+    want[:, 0::2], want[:, 1::2] = zr.real, zr.imag
+    np.testing.assert_allclose(_rot(x, ids), want, rtol=1e-10, atol=1e-10)
+
+
+def test_rope_relative_property():
+    q = RNG.standard_normal(128)
+    k = RNG.standard_normal(128)
+    p = np.array([3, 7, 11, 2], dtype=np.float64)
+    pp = np.array([1, 2, 5, 9], dtype=np.float64)
+    lhs = _rot(q[None], p[None])[0] @ _rot(k[None], pp[None])[0]
+    rhs = _rot(q[None], (p - pp)[None])[0] @ k
+    assert abs(lhs - rhs) < 1e-10
+
+
+def test_rope_axis_ownership_and_adjacent_pairs():
+    # A position on axis a only moves dims [32a, 32a+32); dim 2j's partner is 2j+1.
+    for a in range(4):
+        ids = np.zeros((1, 4)); ids[0, a] = 3.0
+        for d in range(0, 128, 2):
+            e = np.zeros((1, 128)); e[0, d] = 1.0
+            y = _rot(e, ids)[0]
+            nz = set(np.flatnonzero(np.abs(y) > 1e-14).tolist())
+            if a * AXIS <= d < (a + 1) * AXIS:
+                assert nz <= {d, d + 1} and (d + 1 in nz or abs(math.sin(3.0 * THETA ** (-(d - a * AXIS) / AXIS))) < 1e-14)
+            else:
+                assert nz == {d}
+
+
+def test_rope_frequency_ladder_fixes_theta():
+    # Pair j of an axis at position p turns exactly as pair 0 at position p*theta^(-2j/32):
+    # pins theta and the exponent without re-typing the table.
+    p = 1000.0
+    for j in (1, 5, 8, 15):
+        e = np.zeros((1, 128)); e[0, AXIS + 2 * j] = 1.0
+        y = _rot(e, np.array([[0, p, 0, 0]]))[0][AXIS + 2 * j: AXIS + 2 * j + 2]
+        p_eq = p * THETA ** (-2.0 * j / AXIS)
+        z = _rot(np.eye(1, 128), np.array([[p_eq, 0, 0, 0]]))[0][:2]
+        np.testing.assert_allclose(y, z, atol=1e-9)
+    # and theta is the pages' 2000: pair 8 of axis h at position 2000 turns by sqrt(2000)
+    e = np.zeros((1, 128)); e[0, AXIS + 16] = 1.0
+    y = _rot(e, np.array([[0, 2000.0, 0, 0]]))[0][AXIS + 16: AXIS + 18]
+    np.testing.assert_allclose(y, [math.cos(math.sqrt(2000.0)), math.sin(math.sqrt(2000.0))], atol=1e-9)
+
+
+# ------------------------------------------------------------------ norms / activations
+def test_layer_norm_moments():
+    x = RNG.standard_normal((4, 3072)) * 3 + 1.5
+    y = O.layer_norm(x, 1e-6)
+    np.testing.assert_allclose(y.mean(-1), 0, atol=1e-12)
+    var = x.var(-1)
+    np.testing.assert_allclose(y.var(-1), var / (var + 1e-6), rtol=1e-12)
+
+
+def test_adaln_zero_modulation_is_library_layer_norm():
+    x = RNG.standard_normal((3, 257))
+    z = np.zeros((1, 257))
+    want = torch.nn.functional.layer_norm(torch.from_numpy(x), (257,), eps=1e-6).numpy()
+    np.testing.assert_allclose(O.adaln(x, z, z, 1e-6), want, rtol=1e-10, atol=1e-10)
+
+
+def test_adaln_shift_and_one_plus_scale():
+    x = RNG.standard_normal((3, 64))
+    sc = RNG.standard_normal((1, 64))
+    sh = RNG.standard_normal((1, 64))
+    ln = torch.nn.functional.layer_norm(torch.from_numpy(x), (64,), eps=1e-6).numpy()
+    # scale = -1 kills the normalised term entirely, leaving the shift
+    np.testing.assert_allclose(O.adaln(x, sh, -np.ones((1, 64)), 1e-6), np.broadcast_to(sh, x.shape), atol=1e-12)
+    # linear in the shift, affine in the scale with slope LN(x)
+    np.testing.assert_allclose(O.adaln(x, sh, sc, 1e-6) - O.adaln(x, 0 * sh, sc, 1e-6), np.broadcast_to(sh, x.shape), atol=1e-12)
+    np.testing.assert_allclose(O.adaln(x, sh, sc + 1, 1e-6) - O.adaln(x, sh, sc, 1e-6), ln, atol=1e-10)
+
+
+def test_rms_norm_against_library_and_constant_weight():
+    x = RNG.standard_normal((5, 128)) * 4
+    w = RNG.standard_normal(128)
+    want = torch.nn.functional.rms_norm(torch.from_numpy(x), (128,), weight=torch.from_numpy(w), eps=1e-6).numpy()
+    np.testing.assert_allclose(O.rms_norm(x, w, 1e-6), want, rtol=1e-10, atol=1e-10)
+    y = O.rms_norm(x, np.full(128, 2.5), 0.0)
+    np.testing.assert_allclose(np.sqrt((y ** 2).mean(-1)), 2.5, rtol=1e-12)
+
+
+def test_silu_and_swiglu():
+    z = np.linspace(-30, 30, 601)
+    want = torch.nn.functional.silu(torch.from_numpy(z)).numpy()
+    np.testing.assert_allclose(O.silu(z), want, rtol=1e-12, atol=1e-300)
+    assert O.silu(np.array(0.0)) == 0.0
+    g = RNG.standard_normal(10)
+    # the first argument is the gated one: up = 1 leaves silu(gate)
+    np.testing.assert_allclose(O.swiglu(g, np.ones(10)), O.silu(g))
+    np.testing.assert_allclose(O.swiglu(np.full(10, 50.0), g), 50.0 * g)
+
+
+# ------------------------------------------------------------------ attention
+def _brute_attention(q, k, v):
+    N, D = len(q), len(q[0])
+    out = []
+    for i in range(N):
+        w = [math.exp(sum(q[i][d] * k[j][d] for d in range(D)) / math.sqrt(D)) for j in range(N)]
+        tot = sum(w)
+        out.append([sum(w[j] * v[j][d] for j in range(N)) / tot for d in range(D)])
+    return out
+
+
+def test_attention_brute_force_tiny():
+    for N, D in ((1, 4), (5, 8), (9, 16)):
+        q, k, v = (RNG.standard_normal((N, D)) for _ in range(3))
+        got = O.attention(q[None, :, None], k[None, :, None], v[None, :, None])[0, :, 0]
+        np.testing.assert_allclose(got, np.array(_brute_attention(q.tolist(), k.tolist(), v.tolist())), rtol=1e-12, atol=1e-12)
+
+
+def test_attention_against_library_sdpa_and_heads_separate():
+    q, k, v = (torch.randn(2, 3, 37, 128, dtype=torch.float64) for _ in range(3))
+    want = torch.nn.functional.scaled_dot_product_attention(q, k, v).numpy()    # [B, h, N, D]
+    got = O.attention(*(t.permute(0, 2, 1, 3).numpy() for t in (q, k, v)))     # [B, N, h, D]
+    np.testing.assert_allclose(got.transpose(0, 2, 1, 3), want, rtol=1e-10, atol=1e-10)
+
+
+def test_attention_special_cases():
+    N, D = 11, 128
+    v = RNG.standard_normal((N, D))
+    q = RNG.standard_normal((N, D))
+    k = np.tile(RNG.standard_normal((1, D)), (N, 1))      # identical keys -> mean of V
+    got = O.attention(q[None, :, None], k[None, :, None], v[None, :, None])[0, :, 0]
+    np.testing.assert_allclose(got, np.broadcast_to(v.mean(0), got.shape), rtol=1e-12, atol=1e-12)
+    k = np.zeros((N, D)); k[4] = 1e3 * q[0] / np.linalg.norm(q[0])  # one dominant logit
+    got = O.attention(q[:1][None, :, None], k[None, :, None], v[None, :, None])[0, 0, 0]
+    np.testing.assert_allclose(got, v[4], atol=1e-12)
+    # large logits stay finite (row maximum subtracted)
+    qq = RNG.standard_normal((N, D)) * 100
+    assert np.isfinite(O.attention(qq[None, :, None], qq[None, :, None], v[None, :, None])).all()
+
+
+# ------------------------------------------------------------------ timestep / modulation
+def test_sinusoid_closed_forms():
+    e = O.timestep_sinusoid(np.array([0.0]), 256)
+    np.testing.assert_array_equal(e, np.concatenate([np.ones((1, 128)), np.zeros((1, 128))], 1))
+    # sigma = 1e-3 -> tau = 1: element 0 is cos(1), element 128 is sin(1); the last
+    # frequency is 10000^(-127/128)
+    e = O.timestep_sinusoid(np.array([1e-3]), 256)
+    assert abs(e[0, 0] - math.cos(1.0)) < 1e-15 and abs(e[0, 128] - math.sin(1.0)) < 1e-15
+    assert abs(e[0, 255] - math.sin(10000.0 ** (-127.0 / 128.0))) < 1e-15
+
+
+def test_modulation_slots_and_zero_input_path():
+    cfg = O.Config.tiny()
+    H = cfg.hidden
+    w_in = RNG.standard_normal((H, 256)) * 0.02
+    w_out = RNG.standard_normal((H, H)) * 0.02
+    # W_mod picks slot s from a one-hot of e: every slot of m is silu(e) seen through it
+    w_mod = np.zeros((17 * H, H))
+    for s in range(17):
+        w_mod[s * H:(s + 1) * H] = np.eye(H) * (s + 1)
+    m = O.modulation(np.array([0.3, 0.7]), w_in, w_out, w_mod, cfg)
+    parts = O.split_modulation(m, H)
+    assert list(parts)[0] == "img_shift_a" and list(parts)[6] == "txt_shift_a"
+    assert list(parts)[12] == "single_shift" and list(parts)[15] == "final_shift"
+    base = parts["img_shift_a"][:, 0]
+    for s, name in enumerate(parts):
+        np.testing.assert_allclose(parts[name][:, 0], base * (s + 1), rtol=1e-12)
+    # sigma enters only through the sinusoid: equal sigma -> equal rows
+    m2 = O.modulation(np.array([0.5, 0.5]), w_in, w_out, w_mod, cfg)
+    np.testing.assert_array_equal(m2[0], m2[1])
+
+
+# ------------------------------------------------------------------ blocks
+def _tiny_block_setup(seed=0, batch=1, n_txt=8, grid=(3, 4), ref=((2, 2),)):
+    wd = synth.TINY
+    wl = synth.Workload("t", wd, batch, n_txt, grid, ref)
+    g = synth.generator(seed)
+    img, txt = synth.stream_weights(wd, g), synth.stream_weights(wd, g)
+    sgl = synth.single_weights(wd, g)
+    bi = synth.block_inputs(wl, seed)
+    cfg = Hx.oracle_config(wd)
+    ids = O.token_ids(n_txt, grid[0], grid[1], ref)
+    c, s = O.rope_table(ids, cfg.axes_dim, cfg.rope_theta)
+    x = Hx.to_np(bi["x"])
+    m = Hx.to_np(bi["mod"])
+    return cfg, wl, Hx.oracle_stream(img), Hx.oracle_stream(txt), Hx.oracle_single(sgl), x, m, c, s
+
+
+def test_dual_block_zero_gates_leave_residual_unchanged():
+    cfg, wl, wi, wt, ws, x, m, c, s = _tiny_block_setup()
+    H = cfg.hidden
+    m[:, 2 * H:3 * H] = 0; m[:, 5 * H:6 * H] = 0; m[:, 8 * H:9 * H] = 0; m[:, 11 * H:12 * H] = 0
+    y = O.dual_block(x, wl.n_txt, wi, wt, O.split_modulation(m, H), c, s, cfg)
+    np.testing.assert_array_equal(y, x)
+
+
+def test_dual_block_routes_streams_to_their_modulation():
+    cfg, wl, wi, wt, ws, x, m, c, s = _tiny_block_setup()
+    H = cfg.hidden
+    m_img_off = m.copy(); m_img_off[:, 2 * H:3 * H] = 0; m_img_off[:, 5 * H:6 * H] = 0
+    y = O.dual_block(x, wl.n_txt, wi, wt, O.split_modulation(m_img_off, H), c, s, cfg)
+    np.testing.assert_array_equal(y[:, wl.n_txt:], x[:, wl.n_txt:])     # image + reference rows untouched
+    assert np.abs(y[:, :wl.n_txt] - x[:, :wl.n_txt]).max() > 1e-3
+    m_txt_off = m.copy(); m_txt_off[:, 8 * H:9 * H] = 0; m_txt_off[:, 11 * H:12 * H] = 0
+    y = O.dual_block(x, wl.n_txt, wi, wt, O.split_modulation(m_txt_off, H), c, s, cfg)
+    np.testing.assert_array_equal(y[:, :wl.n_txt], x[:, :wl.n_txt])
+    assert np.abs(y[:, wl.n_txt:] - x[:, wl.n_txt:]).max() > 1e-3
+
+
+def test_dual_block_attention_is_joint_and_streams_use_own_weights():
+    cfg, wl, wi, wt, ws, x, m, c, s = _tiny_block_setup()
+    mod = O.split_modulation(m, cfg.hidden)
+    y = O.dual_block(x, wl.n_txt, wi, wt, mod, c, s, cfg)
+    x2 = x.copy(); x2[:, -1] += RNG.standard_normal(x.shape[-1])  # not a constant: LN ignores that                                    # perturb one reference row
+    y2 = O.dual_block(x2, wl.n_txt, wi, wt, mod, c, s, cfg)
+    assert np.abs(y2[:, 0] - y[:, 0]).max() > 1e-6                     # text row sees it
+    # swapping the text weights changes only... everything (joint attention), but the
+    # image rows' MLP uses the image weights: zero image MLP-out -> image rows differ from txt-MLP-zeroed run
+    wi0 = O.StreamWeights(**{**wi.__dict__, "mlp_out": np.zeros_like(wi.mlp_out)})
+    y3 = O.dual_block(x, wl.n_txt, wi0, wt, mod, c, s, cfg)
+    np.testing.assert_array_equal(y3[:, :wl.n_txt], y[:, :wl.n_txt])
+    assert np.abs(y3[:, wl.n_txt:] - y[:, wl.n_txt:]).max() > 1e-4
+
+
+def test_single_block_zero_gate_and_permutation_equivariance():
+    cfg, wl, wi, wt, ws, x, m, c, s = _tiny_block_setup(ref=())
+    H = cfg.hidden
+    m0 = m.copy(); m0[:, 14 * H:15 * H] = 0
+    np.testing.assert_array_equal(O.single_block(x, ws, O.split_modulation(m0, H), c, s, cfg), x)
+    # with every id equal, RoPE is one rotation for all rows: permuting rows permutes outputs
+    ids = np.zeros((x.shape[1], 4)); ids[:, 1] = 5
+    c1, s1 = O.rope_table(ids)
+    mod = O.split_modulation(m, H)
+    perm = RNG.permutation(x.shape[1])
+    y = O.single_block(x, ws, mod, c1, s1, cfg)
+    yp = O.single_block(x[:, perm], ws, mod, c1, s1, cfg)
+    np.testing.assert_allclose(yp, y[:, perm], rtol=1e-10, atol=1e-10)
+
+
+def test_blocks_batch_rows_independent():
+    cfg, wl, wi, wt, ws, x, m, c, s = _tiny_block_setup(batch=3)
+    mod = O.split_modulation(m, cfg.hidden)
+    y = O.dual_block(x, wl.n_txt, wi, wt, mod, c, s, cfg)
+    y1 = O.dual_block(x[1:2], wl.n_txt, wi, wt, O.split_modulation(m[1:2], cfg.hidden), c, s, cfg)
+    np.testing.assert_allclose(y[1:2], y1, rtol=1e-13, atol=1e-13)
+    z = O.single_block(x, ws, mod, c, s, cfg)
+    z1 = O.single_block(x[2:3], ws, O.split_modulation(m[2:3], cfg.hidden), c, s, cfg)
+    np.testing.assert_allclose(z[2:3], z1, rtol=1e-13, atol=1e-13)
+
+
+# ------------------------------------------------------------------ whole step / loop
+def _tiny_step():
+    wd = synth.TINY
+    wl = synth.Workload("t", wd, 2, 16, (4, 4), ((2, 3),))
+    w = synth.model_weights(wd, seed=5)
+    inp = synth.step_inputs(wl, seed=5)
+    ids = O.token_ids(wl.n_txt, *wl.grid, wl.ref_grids)
+    return wd, wl, w, inp, ids
+
+
+def test_step_fp32_agrees_with_fp64():
+    wd, wl, w, inp, ids = _tiny_step()
+    args = [Hx.to_np(inp["img_tokens"]), Hx.to_np(inp["ref_tokens"]), Hx.to_np(inp["txt_emb"]),
+            Hx.to_np(inp["sigma"]), ids]
+    v64 = O.dit_step(Hx.oracle_weights(wd, w, np.float64), *args, dtype=np.float64)
+    v32 = O.dit_step(Hx.oracle_weights(wd, w, np.float32), *[a.astype(np.float32) if a.dtype != np.int32 else a for a in args], dtype=np.float32)
+    assert v64.shape == (2, 16, 128)
+    assert Hx.cosine(v32, v64) > 0.99999
+
+
+def test_step_uses_only_target_rows_and_ref_tokens_matter():
+    wd, wl, w, inp, ids = _tiny_step()
+    ow = Hx.oracle_weights(wd, w)
+    a = [Hx.to_np(inp["img_tokens"]), Hx.to_np(inp["ref_tokens"]), Hx.to_np(inp["txt_emb"]), Hx.to_np(inp["sigma"]), ids]
+    v = O.dit_step(ow, *a)
+    a2 = list(a); a2[1] = a[1] + 1.0
+    v2 = O.dit_step(ow, *a2)
+    assert v.shape == v2.shape and np.abs(v - v2).max() > 1e-6
+
+
+def test_euler_loop_telescopes_and_schedule_ends_at_zero():
+    sig = O.sigma_schedule(0.8, int(STRUCT["steps"]))
+    assert len(sig) == 5 and sig[0] == 0.8 and sig[-1] == 0.0
+    x = RNG.standard_normal((2, 3))
+    v = RNG.standard_normal((2, 3))
+    y = x
+    for k in range(4):
+        y = O.euler_update(y, v, sig[k], sig[k + 1])
+    np.testing.assert_allclose(y, x - 0.8 * v, rtol=1e-13, atol=1e-13)
+
+
+def test_klein_parameter_count_is_about_4b():
+    # no biases anywhere (reading R17) gives the card's "4B" at klein width
+    w = synth.model_weights(synth.KLEIN, seed=0, device="meta")
+    n = sum(t.numel() for t in [w["mod"]["t_in"], w["mod"]["t_out"], w["mod"]["mod"], w["x_emb"], w["ctx_emb"], w["proj_out"]])
+    n += sum(t.numel() for a, b in w["dual"] for t in list(a.values()) + list(b.values()))
+    n += sum(t.numel() for s in w["single"] for t in s.values())
+    billions = n / 1e9
+    assert abs(billions - float(STRUCT["model_params_billion"])) < 0.25, billions
+    assert len(w["dual"]) == int(STRUCT["n_dual"]) and len(w["single"]) == int(STRUCT["n_single"])
+    assert synth.KLEIN.txt_dim == int(STRUCT["text_dim"]) == 3 * 2560
