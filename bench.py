@@ -1,0 +1,410 @@
+"""Benchmark of one FLUX.2 [klein]-style DiT denoising step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+One "step" is one pass of the whole hot path (modulation, embedders, 5 dual-stream and
+20 single-stream blocks, final layer) over one batch of synthetic input, through the
+C ABI (dit_step_fwd).  The default workload is the 1024x1024 step (512 text + 4096 image
+tokens, batch 1).  Prints ONE JSON line on rank 0.
+
+  value      steps/s over the timed region, device-resident inputs (CUDA events on the
+             launching stream, synchronised on both sides, max over ranks)
+  e2e        the same metric through dit_step_host: pinned host inputs copied in and the
+             velocity copied out inside the timed region
+  roofline   the dominant kernel class (most device time in the timed region): its
+             algorithmic FLOPs per launch / its mean launch time, measured live with CUDA
+             events recorded around each launch on its own stream
+  cpu_baseline  the CPU oracle (fp32 numpy) timed on a bounded sample (one dual-stream and
+             one single-stream block at the same shape), scaled to the 5 + 20 blocks
+  --impl reference  times the CPU oracle as the reference arm (rank 0 only).
+
+Weights are seeded random (no trained checkpoint exists here); the step streams 7.4 GB
+of weights per step, far larger than the 129 MB L2, so no L2 flush is needed between
+timed steps.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "DiT steps/s at 1024² (512 txt + 4096 img tokens); TFLOP/s vs GB300 bf16 peak"
+UNIT = "steps/s"
+
+# Roofline denominators: the measured peaks of this GPU pool when the driver has written
+# them, else the recipe's fallback figures (reported as such).
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM traffic per launch of the dominant kernel from one ncu capture (see profiles/);
+# None until captured for the current kernel.
+NCU_TRAFFIC = {}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            return d, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK), "fallback"
+
+
+def peak_get(peaks, *names):
+    for n in names:
+        if n in peaks and isinstance(peaks[n], (int, float)):
+            return float(peaks[n])
+    return None
+
+
+# ---------------------------------------------------------------------------------- FLOPs
+def class_flops(wd, batch, n_txt, n_img, n_ref):
+    """Algorithmic FLOPs (multiply-add = 2) of one launch of each kernel class."""
+    H, F, C = wd.hidden, wd.mlp_hidden, wd.in_channels
+    N = n_txt + n_img + n_ref
+    M = batch * N
+    return {
+        "gemm_qkv_rmsnorm_rope": 2.0 * M * H * 3 * H,
+        "gemm_fused_qkv_mlp": 2.0 * M * H * (3 * H + 2 * F),
+        "gemm_dual_out_proj": 2.0 * M * H * H,
+        "gemm_swiglu": 2.0 * M * H * 2 * F,
+        "gemm_dual_mlp_out": 2.0 * M * F * H,
+        "gemm_single_out_proj": 2.0 * M * (H + F) * H,
+        "attention": 4.0 * batch * N * N * H,
+    }
+
+
+def step_flops(wd, batch, n_txt, n_img, n_ref):
+    H, F, C = wd.hidden, wd.mlp_hidden, wd.in_channels
+    N = n_txt + n_img + n_ref
+    blk = 2.0 * N * H * (4 * H + 3 * F) + 4.0 * N * N * H
+    embed = 2.0 * (n_img + n_ref) * C * H + 2.0 * n_txt * wd.txt_dim * H + 2.0 * n_img * H * C
+    return batch * ((wd.n_dual + wd.n_single) * blk + embed)
+
+
+# ---------------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) of SM clock and throttle reasons while running."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu_id), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_id_for_smi(torch, dev_index):
+    try:
+        u = str(torch.cuda.get_device_properties(dev_index).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return dev_index
+
+
+# ---------------------------------------------------------------------------------- CPU oracle
+def oracle_block_times(wl, seed=0, reps=1):
+    """Seconds of one dual-stream and one single-stream block of the fp32 oracle at wl's shape."""
+    import numpy as np
+    import torch
+    from diffusion_transformer_step_gb300 import synth
+    from oracle import dit_oracle as O
+
+    wd = wl.widths
+    g = synth.generator(seed)
+    img, txt, sgl = synth.stream_weights(wd, g), synth.stream_weights(wd, g), synth.single_weights(wd, g)
+    bi = synth.block_inputs(synth.Workload("b1", wd, 1, wl.n_txt, wl.grid, wl.ref_grids), seed)
+    f = lambda t: t.float().numpy()
+    cfg = O.Config(hidden=wd.hidden, heads=wd.heads, head_dim=wd.head_dim, mlp_hidden=wd.mlp_hidden)
+    sw = lambda d: O.StreamWeights(**{k: f(v) for k, v in d.items()})
+    c, s = O.rope_table(O.token_ids(wl.n_txt, *wl.grid, wl.ref_grids))
+    c, s = c.astype(np.float32), s.astype(np.float32)
+    x, m = f(bi["x"]), O.split_modulation(f(bi["mod"]), wd.hidden)
+    wi, wt, ws = sw(img), sw(txt), O.SingleWeights(**{k: f(v) for k, v in sgl.items()})
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        O.dual_block(x, wl.n_txt, wi, wt, m, c, s, cfg, np.float32)
+    t1 = time.perf_counter()
+    for _ in range(reps):
+        O.single_block(x, ws, m, c, s, cfg, np.float32)
+    t2 = time.perf_counter()
+    return (t1 - t0) / reps, (t2 - t1) / reps
+
+
+def cpu_cores():
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return os.cpu_count()
+
+
+# ---------------------------------------------------------------------------------- arms
+def run_reference(args, wl):
+    """The CPU oracle as the reference arm: each step is a bounded sample (one single-stream
+    block of the same shape, fp32), scaled to the step's 25 blocks."""
+    from oracle import dit_oracle as O  # noqa: F401  (the one other place bench runs the oracle)
+    import numpy as np
+    import torch
+    from diffusion_transformer_step_gb300 import synth
+    from oracle import dit_oracle as Ox
+
+    wd = wl.widths
+    g = synth.generator(0)
+    sgl = synth.single_weights(wd, g)
+    bi = synth.block_inputs(synth.Workload("b1", wd, 1, wl.n_txt, wl.grid, wl.ref_grids), 0)
+    f = lambda t: t.float().numpy()
+    cfg = Ox.Config(hidden=wd.hidden, heads=wd.heads, head_dim=wd.head_dim, mlp_hidden=wd.mlp_hidden)
+    c, s = Ox.rope_table(Ox.token_ids(wl.n_txt, *wl.grid, wl.ref_grids))
+    c, s = c.astype(np.float32), s.astype(np.float32)
+    x, m = f(bi["x"]), Ox.split_modulation(f(bi["mod"]), wd.hidden)
+    ws = Ox.SingleWeights(**{k: f(v) for k, v in sgl.items()})
+    for _ in range(args.warmup):
+        Ox.single_block(x, ws, m, c, s, cfg, np.float32)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        Ox.single_block(x, ws, m, c, s, cfg, np.float32)
+    dt = (time.perf_counter() - t0) / args.steps
+    step_s = dt * (wd.n_dual + wd.n_single)
+    value = wl.batch / step_s
+    flops = step_flops(wd, wl.batch, wl.n_txt, wl.n_img, wl.n_ref)
+    sample = f"one single-stream block of the {wl.name} shape per step (fp32 numpy oracle), x{wd.n_dual + wd.n_single} blocks"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": workload_config(wl), "tflops": flops / step_s / 1e12,
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(wl):
+    return {"workload": wl.name, "batch": wl.batch, "n_txt": wl.n_txt, "n_img": wl.n_img, "n_ref": wl.n_ref,
+            "seq_len": wl.n_tokens, "grid": list(wl.grid), "ref_grids": [list(g) for g in wl.ref_grids],
+            "l2": "inputs larger than L2 (7.4 GB of bf16 weights streamed per step), no flush",
+            "parallelism": "replicas (batch rows per GPU)"}
+
+
+def run_ours(args, wl, rank, world, local_rank):
+    import torch
+    import torch.distributed as tdist
+    from diffusion_transformer_step_gb300 import build_lib, dit, synth
+
+    build_lib.build()
+    dev = f"cuda:{local_rank}"
+    torch.cuda.set_device(local_rank)
+    wd = wl.widths
+    logical = synth.model_weights(wd, seed=rank, device=dev)
+    W = dit.DeviceWeights(wd, logical, device=dev)
+    del logical
+    inp = synth.step_inputs(wl, seed=rank, device=dev)
+    shape = dit.make_shape(wl.batch, wl.n_txt, wl.n_img, wl.n_ref)
+    ids = dit.dit_token_ids(shape, *wl.grid, wl.ref_grids)
+    N = wl.n_tokens
+    rope = torch.empty((N, 64, 2), dtype=torch.float32, device=dev)
+    dit.dit_rope_table(W.cfg, ids.to(dev), N, rope)
+    nbytes = dit.dit_workspace_size(W.cfg, shape)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+    vel = torch.empty((wl.batch, wl.n_img, wd.in_channels), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+    ref = inp["ref_tokens"]
+
+    def step():
+        dit.dit_step_fwd(W.w, shape, inp["img_tokens"], ref, inp["txt_emb"], rope, inp["sigma"], vel, ws, nbytes,
+                         stream)
+
+    def barrier():
+        if world > 1:
+            tdist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    st, where = dit.dit_sync_status(ws, stream)
+    if st != dit.DIT_OK:
+        raise RuntimeError(f"device wait gave up during warm-up at site {where:#x}")
+
+    # ---- timed region (device-resident inputs), with per-launch events for the roofline
+    sampler = ClockSampler(gpu_id_for_smi(torch, local_rank))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = dit.dit_launch_count()
+    per_step_launches = None
+    barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    dit.dit_timing_begin(args.steps * 200)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    records = dit.dit_timing_end(args.steps * 200)
+    barrier()
+    launches = dit.dit_launch_count() - launches0
+    ms_total = e0.elapsed_time(e1)
+    st, where = dit.dit_sync_status(ws, stream)
+    if st != dit.DIT_OK:
+        raise RuntimeError(f"device wait gave up in the timed region at site {where:#x}")
+    ms = torch.tensor([ms_total], dtype=torch.float64, device=dev)
+    if world > 1:
+        tdist.all_reduce(ms, op=tdist.ReduceOp.MAX)
+    ms_step = ms.item() / args.steps
+    value = world * wl.batch / (ms_step / 1e3) / wl.batch  # steps/s, all replicas
+
+    # ---- e2e through the host-buffer entry point
+    pin = lambda t: t.detach().to("cpu").contiguous().pin_memory() if t is not None else None
+    h_img, h_ref, h_txt, h_sig = pin(inp["img_tokens"]), pin(ref), pin(inp["txt_emb"]), pin(inp["sigma"])
+    h_vel = torch.empty(tuple(vel.shape), dtype=torch.bfloat16).pin_memory()
+    for _ in range(max(1, args.warmup // 2)):
+        dit.dit_step_host(W.w, shape, h_img, h_ref, h_txt, rope, h_sig, h_vel, ws, nbytes, stream)
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    k_e2e = max(3, args.steps // 2)
+    for _ in range(k_e2e):
+        dit.dit_step_host(W.w, shape, h_img, h_ref, h_txt, rope, h_sig, h_vel, ws, nbytes, stream)
+        stream.synchronize()  # the caller reads the velocity every step
+    e2e_s = (time.perf_counter() - t0) / k_e2e
+    tt = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
+    if world > 1:
+        tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
+    e2e_s = tt.item()
+    h2d = sum(t.numel() * t.element_size() for t in (h_img, h_ref, h_txt, h_sig) if t is not None)
+    d2h = h_vel.numel() * h_vel.element_size()
+
+    if rank != 0:
+        return
+
+    # ---- roofline of the dominant kernel class
+    peaks, src = load_peaks()
+    flops_cls = class_flops(wd, wl.batch, wl.n_txt, wl.n_img, wl.n_ref)
+    by_cls = {}
+    for name, t in records:
+        by_cls.setdefault(name, []).append(t)
+    total_rec = sum(sum(v) for v in by_cls.values())
+    kernels = {k: {"launches": len(v), "ms_total": round(sum(v), 4), "ms_mean": round(sum(v) / len(v), 5),
+                   "share": round(sum(v) / total_rec, 4) if total_rec else None} for k, v in by_cls.items()}
+    for k, v in kernels.items():
+        if k in flops_cls:
+            v["tflops"] = round(flops_cls[k] / (v["ms_mean"] / 1e3) / 1e12, 1)
+    dom = max((k for k in by_cls if k in flops_cls), key=lambda k: sum(by_cls[k]))
+    mean_ms = sum(by_cls[dom]) / len(by_cls[dom])
+    achieved = flops_cls[dom] / (mean_ms / 1e3) / 1e12
+    peak = peak_get(peaks, "bf16_tflops_sustained", "bf16_tflops")
+    tr = NCU_TRAFFIC.get(dom)
+    roofline = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "peak_source": f"bf16 sustained, of {src}",
+                "traffic": tr, "flops_per_launch": flops_cls[dom], "launch_ms_mean": round(mean_ms, 4)}
+    flops = step_flops(wd, wl.batch, wl.n_txt, wl.n_img, wl.n_ref)
+    tflops = flops / (ms_step / 1e3) / 1e12
+
+    # ---- CPU oracle baseline on a bounded sample
+    cpu = None
+    if not args.no_cpu_baseline:
+        td, ts = oracle_block_times(wl)
+        step_s = wd.n_dual * td + wd.n_single * ts
+        cpu = {"value": wl.batch / step_s / wl.batch, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"one dual-stream ({td:.2f} s) and one single-stream ({ts:.2f} s) block of the "
+                         f"{wl.name} shape, fp32 numpy oracle, scaled to {wd.n_dual}+{wd.n_single} blocks"}
+
+    line = {"metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded random weights and inputs)",
+            "config": workload_config(wl),
+            "tflops": round(tflops, 1),
+            "frac_of_bf16_peak": {"measured_or_fallback": src,
+                                  "burst": round(tflops / peak_get(peaks, "bf16_tflops", "bf16_tflops_sustained"), 4),
+                                  "sustained": round(tflops / peak, 4), "nominal_2250": round(tflops / 2250.0, 4)},
+            "roofline": roofline, "kernels": kernels,
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(world / e2e_s, 4), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches, "clocks": clocks}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="step_1024")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    from diffusion_transformer_step_gb300 import synth
+    wl = synth.WORKLOADS[args.workload]
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, wl)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(local_rank)
+        tdist.init_process_group("nccl")
+    try:
+        run_ours(args, wl, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as tdist
+            tdist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

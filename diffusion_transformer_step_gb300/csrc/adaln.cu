@@ -1,0 +1,129 @@
+// Adaptive LayerNorm with the per-step shift/scale: y = (1 + scale) LN(x) + shift.
+// LayerNorm over the hidden dim without affine, biased variance, fp32 statistics
+// (readings R3, R4).  Input rows are bf16, or fp32 for the dual-stream block's
+// intermediate residual stream.  One warp per row: 128-bit loads, the row kept in registers, a
+// two-pass mean / variance with warp-shuffle reductions.  HBM-bound: each row is read
+// once (2H bytes) and written once (2H bytes); the modulation vectors stay in L1/L2.
+#include "runtime.h"
+
+namespace dit {
+
+namespace {
+
+constexpr int kRowsPerBlock = 8;  // 8 warps
+
+template <int VPL, bool F32IN>  // 8-element vectors per lane: hidden = VPL * 256
+__global__ void __launch_bounds__(kRowsPerBlock * 32) adaln_kernel(AdaLNArgs a) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long row = (long long)blockIdx.x * kRowsPerBlock + warp;
+  const long long total = (long long)a.batch * a.rows;
+  if (row >= total) return;
+  const int b = (int)(row / a.rows);
+  const int r = (int)(row - (long long)b * a.rows);
+  const int H = VPL * 256;
+
+  const long long xoff = b * a.x_bstride + (long long)(a.x_row0 + r) * H;
+  const uint4* xv = reinterpret_cast<const uint4*>(reinterpret_cast<const bf16*>(a.x) + xoff);
+  const float4* xf = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.x) + xoff);
+  uint4* yv = reinterpret_cast<uint4*>(a.y + b * a.y_bstride + (long long)r * H);
+  const bool lo = r < a.split;
+  const uint4* shv = reinterpret_cast<const uint4*>((lo ? a.shift_lo : a.shift_hi) + b * a.mod_stride);
+  const uint4* scv = reinterpret_cast<const uint4*>((lo ? a.scale_lo : a.scale_hi) + b * a.mod_stride);
+
+  float v[VPL][8];
+  float sum = 0.f;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    if (F32IN) {
+      const float4 f0 = __ldg(xf + 2 * (i * 32 + lane)), f1 = __ldg(xf + 2 * (i * 32 + lane) + 1);
+      v[i][0] = f0.x; v[i][1] = f0.y; v[i][2] = f0.z; v[i][3] = f0.w;
+      v[i][4] = f1.x; v[i][5] = f1.y; v[i][6] = f1.z; v[i][7] = f1.w;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) sum += v[i][j];
+    } else {
+      const uint4 u = __ldg(xv + i * 32 + lane);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 f = unpack_bf16x2(w[j]);
+        v[i][2 * j] = f.x;
+        v[i][2 * j + 1] = f.y;
+        sum += f.x + f.y;
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  const float mean = sum * (1.0f / H);
+  float sq = 0.f;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float d = v[i][j] - mean;
+      sq += d * d;
+    }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+  const float rstd = rsqrtf(sq * (1.0f / H) + a.eps);
+
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const uint4 sh = __ldg(shv + i * 32 + lane);
+    const uint4 sc = __ldg(scv + i * 32 + lane);
+    const uint32_t shw[4] = {sh.x, sh.y, sh.z, sh.w};
+    const uint32_t scw[4] = {sc.x, sc.y, sc.z, sc.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 s2 = unpack_bf16x2(shw[j]);
+      const float2 c2 = unpack_bf16x2(scw[j]);
+      const float y0 = (1.0f + c2.x) * ((v[i][2 * j] - mean) * rstd) + s2.x;
+      const float y1 = (1.0f + c2.y) * ((v[i][2 * j + 1] - mean) * rstd) + s2.y;
+      o[j] = pack_bf16x2(y0, y1);
+    }
+    yv[i * 32 + lane] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+template <int VPL>
+cudaError_t launch_vpl(const AdaLNArgs& a, cudaStream_t s) {
+  const long long total = (long long)a.batch * a.rows;
+  const unsigned grid = (unsigned)((total + kRowsPerBlock - 1) / kRowsPerBlock);
+  LaunchScope scope(kClsAdaLN, s);
+  if (a.x_f32)
+    adaln_kernel<VPL, true><<<grid, kRowsPerBlock * 32, 0, s>>>(a);
+  else
+    adaln_kernel<VPL, false><<<grid, kRowsPerBlock * 32, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool adaln_supports(int hidden) {
+  if (hidden <= 0 || hidden % 256 != 0) return false;
+  switch (hidden / 256) {
+    case 1: case 2: case 3: case 4: case 5: case 6: case 8: case 10: case 12: case 14: case 16: return true;
+    default: return false;
+  }
+}
+
+cudaError_t launch_adaln(const AdaLNArgs& a, cudaStream_t s) {
+  if ((long long)a.batch * a.rows == 0) return cudaSuccess;
+  switch (a.hidden / 256) {
+    case 1: return launch_vpl<1>(a, s);
+    case 2: return launch_vpl<2>(a, s);
+    case 3: return launch_vpl<3>(a, s);
+    case 4: return launch_vpl<4>(a, s);
+    case 5: return launch_vpl<5>(a, s);
+    case 6: return launch_vpl<6>(a, s);
+    case 8: return launch_vpl<8>(a, s);
+    case 10: return launch_vpl<10>(a, s);
+    case 12: return launch_vpl<12>(a, s);
+    case 14: return launch_vpl<14>(a, s);
+    case 16: return launch_vpl<16>(a, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace dit

@@ -1,0 +1,675 @@
+// The C ABI (include/dit.h): argument validation, workspace layout, the launch
+// sequence of a dual-stream block, a single-stream block and the whole step, and the
+// host runtime pieces (launch accounting, per-launch timing, TMA descriptor encoding).
+#include <atomic>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/dit.h"
+#include "runtime.h"
+
+namespace dit {
+
+// ---------------------------------------------------------------------------------
+// Launch accounting and timing
+// ---------------------------------------------------------------------------------
+namespace {
+std::atomic<unsigned long long> g_launches{0};
+std::mutex g_timing_mu;
+bool g_timing_on = false;
+struct TimingRec {
+  int cls;
+  cudaEvent_t start, stop;
+};
+std::vector<TimingRec> g_recs;
+int g_rec_used = 0;
+}  // namespace
+
+const char* kernel_class_name(int cls) {
+  static const char* names[kClsCount] = {
+      "adaln",          "gemm_qkv_rmsnorm_rope", "gemm_fused_qkv_mlp",  "gemm_gated_residual",
+      "gemm_swiglu",    "gemm_plain",            "attention",           "modulation_gemv",
+      "rope_table",     "pack_mlp_in",           "gemm_dual_out_proj",  "gemm_dual_mlp_out",
+      "gemm_single_out_proj"};
+  return (cls >= 0 && cls < kClsCount) ? names[cls] : "?";
+}
+
+LaunchScope::LaunchScope(int cls, cudaStream_t stream) : slot_(-1), stream_(stream) {
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  std::lock_guard<std::mutex> lk(g_timing_mu);
+  if (g_timing_on && g_rec_used < (int)g_recs.size()) {
+    slot_ = g_rec_used++;
+    g_recs[slot_].cls = cls;
+    cudaEventRecord(g_recs[slot_].start, stream);
+  }
+}
+
+LaunchScope::~LaunchScope() {
+  if (slot_ >= 0) cudaEventRecord(g_recs[slot_].stop, stream_);
+}
+
+int sm_count() {
+  static int cached[16] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 16 && cached[dev]) return cached[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+  if (dev >= 0 && dev < 16) cached[dev] = n;
+  return n;
+}
+
+bool encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                      const uint64_t* strides_bytes, const uint32_t* box) {
+  typedef CUresult (*EncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                               const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                               CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  static EncodeFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(p);
+  });
+  if (!fn) return false;
+  cuuint64_t d[5];
+  cuuint64_t st[4];
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+  }
+  for (int i = 0; i + 1 < rank; ++i) st[i] = strides_bytes[i];
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), d, st, bx,
+                        es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------------------------
+// Validation and workspace layout
+// ---------------------------------------------------------------------------------
+namespace {
+
+constexpr int kMaxBatch = 64;
+constexpr long long kMaxTokens = 1 << 20;
+
+inline bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+dit_status check_config(const dit_config* c) {
+  if (!c) return DIT_ERR_INVALID_ARG;
+  if (c->head_dim != 128 || c->heads <= 0 || c->hidden != c->heads * 128) return DIT_ERR_UNSUPPORTED;
+  if (!adaln_supports(c->hidden)) return DIT_ERR_UNSUPPORTED;
+  if (c->mlp_hidden <= 0 || c->mlp_hidden % 128 != 0) return DIT_ERR_UNSUPPORTED;
+  if (c->in_channels <= 0 || c->in_channels % 32 != 0) return DIT_ERR_UNSUPPORTED;
+  if (c->txt_dim <= 0 || c->txt_dim % 8 != 0) return DIT_ERR_UNSUPPORTED;
+  if (c->n_dual < 0 || c->n_single < 0) return DIT_ERR_INVALID_ARG;
+  int sum = 0;
+  for (int i = 0; i < 4; ++i) {
+    if (c->axes_dim[i] < 0 || c->axes_dim[i] % 2 != 0) return DIT_ERR_UNSUPPORTED;
+    sum += c->axes_dim[i];
+  }
+  if (sum != c->head_dim) return DIT_ERR_UNSUPPORTED;
+  if (!(c->rope_theta > 0.f) || !(c->eps > 0.f)) return DIT_ERR_INVALID_ARG;
+  return DIT_OK;
+}
+
+dit_status check_shape(const dit_shape* s) {
+  if (!s) return DIT_ERR_INVALID_ARG;
+  if (s->batch < 1 || s->batch > kMaxBatch) return DIT_ERR_INVALID_ARG;
+  if (s->n_txt < 1 || s->n_img < 1 || s->n_ref < 0) return DIT_ERR_INVALID_ARG;
+  if ((long long)s->n_txt + s->n_img + s->n_ref > kMaxTokens) return DIT_ERR_UNSUPPORTED;
+  return DIT_OK;
+}
+
+inline size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct Layout {
+  size_t status, h1, h2, mod, x, x1, y, q, k, v, cat;
+  size_t in_img, in_ref, in_txt, in_sigma, out_vel;
+  size_t block_end, step_end, total;
+};
+
+Layout layout(const dit_config& c, const dit_shape& s) {
+  const size_t B = s.batch, N = (size_t)s.n_txt + s.n_img + s.n_ref, H = c.hidden, F = c.mlp_hidden;
+  Layout L;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = up256(o + bytes);
+    return at;
+  };
+  L.status = take(sizeof(DeviceStatus));
+  L.h1 = take(B * H * 4);
+  L.h2 = take(B * H * 4);
+  L.y = take(B * N * H * 2);
+  L.q = take(B * N * H * 2);
+  L.k = take(B * N * H * 2);
+  L.v = take(B * N * H * 2);
+  L.cat = take(B * N * (H + F) * 2);
+  L.x1 = take(B * N * H * 4);
+  L.block_end = o;
+  L.mod = take(B * 17 * H * 2);
+  L.x = take(B * N * H * 2);
+  L.step_end = o;
+  L.in_img = take(B * (size_t)s.n_img * c.in_channels * 2);
+  L.in_ref = take(B * (size_t)s.n_ref * c.in_channels * 2);
+  L.in_txt = take(B * (size_t)s.n_txt * c.txt_dim * 2);
+  L.in_sigma = take(B * 4);
+  L.out_vel = take(B * (size_t)s.n_img * c.in_channels * 2);
+  L.total = o;
+  return L;
+}
+
+inline uint8_t* at(void* ws, size_t off) { return reinterpret_cast<uint8_t*>(ws) + off; }
+inline bf16* bat(void* ws, size_t off) { return reinterpret_cast<bf16*>(at(ws, off)); }
+inline DeviceStatus* status_of(void* ws) { return reinterpret_cast<DeviceStatus*>(ws); }
+
+inline dit_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DIT_OK : DIT_ERR_CUDA; }
+
+#define DIT_TRY(expr)                     \
+  do {                                    \
+    const dit_status st_ = (expr);        \
+    if (st_ != DIT_OK) return st_;        \
+  } while (0)
+#define DIT_CUDA(expr) DIT_TRY(cuda_status(expr))
+
+dit_status check_stream_weights(const dit_stream_weights& w) {
+  if (!aligned16(w.qkv) || !aligned16(w.q_norm) || !aligned16(w.k_norm) || !aligned16(w.out) ||
+      !aligned16(w.mlp_in) || !aligned16(w.mlp_out))
+    return DIT_ERR_INVALID_ARG;
+  return DIT_OK;
+}
+
+dit_status check_block_args(const dit_weights* w, const dit_shape* shape, const void* x, const void* mod,
+                            const float* rope, void* ws, size_t ws_bytes) {
+  if (!w) return DIT_ERR_INVALID_ARG;
+  DIT_TRY(check_config(&w->cfg));
+  DIT_TRY(check_shape(shape));
+  if (!aligned16(x) || !aligned16(mod) || !aligned16(rope) || !aligned16(ws)) return DIT_ERR_INVALID_ARG;
+  if (ws_bytes < layout(w->cfg, *shape).block_end) return DIT_ERR_WORKSPACE;
+  return DIT_OK;
+}
+
+// Modulation slot offsets (in units of H): img-dual 0..5, txt-dual 6..11, single 12..14,
+// final 15..16.
+enum { kImg = 0, kTxt = 6, kSingle = 12, kFinal = 15 };
+enum { kShiftA = 0, kScaleA = 1, kGateA = 2, kShiftM = 3, kScaleM = 4, kGateM = 5 };
+
+GemmProblemHost blank_problem() {
+  GemmProblemHost p;
+  memset(&p, 0, sizeof(p));
+  return p;
+}
+
+dit_status run_dual_block(const dit_weights* w, int layer, const dit_shape* s, bf16* x, const bf16* mod,
+                          const float* rope, void* ws, cudaStream_t st) {
+  const dit_config& c = w->cfg;
+  const dit_dual_weights& dw = w->dual[layer];
+  const int B = s->batch, N = s->n_txt + s->n_img + s->n_ref, H = c.hidden, F = c.mlp_hidden;
+  const int n_txt = s->n_txt, n_imgref = N - n_txt;
+  const Layout L = layout(c, *s);
+  bf16 *y = bat(ws, L.y), *q = bat(ws, L.q), *k = bat(ws, L.k), *v = bat(ws, L.v), *cat = bat(ws, L.cat);
+  float* x1 = reinterpret_cast<float*>(at(ws, L.x1));  // fp32 residual stream between the two halves
+  DeviceStatus* dst = status_of(ws);
+  const long long ms = 17LL * H;
+  auto slot = [&](int base, int which) { return mod + (long long)(base + which) * H; };
+
+  // 1. y = adaLN(x) with each stream's attention shift / scale
+  AdaLNArgs a1{B, N, H, x, 0, (long long)N * H, 0, y, (long long)N * H, n_txt,
+               slot(kTxt, kShiftA), slot(kTxt, kScaleA), slot(kImg, kShiftA), slot(kImg, kScaleA), ms, c.eps};
+  DIT_CUDA(launch_adaln(a1, st));
+
+  // 2. per-stream QKV projection + QK-RMSNorm + RoPE, head-major Q/K/V
+  GemmProblemHost p[2];
+  const dit_stream_weights* sw[2] = {&dw.txt, &dw.img};
+  const int row0[2] = {0, n_txt}, rows[2] = {n_txt, n_imgref};
+  for (int i = 0; i < 2; ++i) {
+    p[i] = blank_problem();
+    p[i].a = y; p[i].a_rows_total = N; p[i].lda = H; p[i].a_row0 = row0[i]; p[i].rows = rows[i];
+    p[i].w = (const bf16*)sw[i]->qkv; p[i].n = 3 * H; p[i].k = H; p[i].epi = kEpiQKV;
+    p[i].n_qkv = 3 * H; p[i].hidden = H; p[i].q = q; p[i].kk = k; p[i].v = v;
+    p[i].q_norm = (const bf16*)sw[i]->q_norm; p[i].k_norm = (const bf16*)sw[i]->k_norm;
+    p[i].rope = rope; p[i].seq = N; p[i].tok0 = row0[i];
+  }
+  DIT_CUDA(launch_gemm(p, 2, B, c.eps, dst, kClsGemmQKV, st));
+
+  // 3. joint attention over all N rows -> cat[:, :, 0:H]
+  DIT_CUDA(launch_attention(B, c.heads, N, q, k, v, cat, H + F, dst, st));
+
+  // 4. x1 = x + gate_a * (attn out^T), per stream; x1 kept in fp32 so the block rounds
+  //    the residual stream to bf16 once
+  const int gate_a[2] = {kTxt + kGateA, kImg + kGateA};
+  for (int i = 0; i < 2; ++i) {
+    p[i] = blank_problem();
+    p[i].a = cat; p[i].a_rows_total = N; p[i].lda = H + F; p[i].a_row0 = row0[i]; p[i].rows = rows[i];
+    p[i].w = (const bf16*)sw[i]->out; p[i].n = H; p[i].k = H; p[i].epi = kEpiResidual;
+    p[i].res = x; p[i].out_f32 = x1; p[i].out_bstride = (long long)N * H; p[i].ld_out = H; p[i].out_row0 = row0[i];
+    p[i].gate = mod + (long long)gate_a[i] * H; p[i].gate_stride = ms;
+  }
+  DIT_CUDA(launch_gemm(p, 2, B, c.eps, dst, kClsGemmDualOut, st));
+
+  // 5. y = adaLN(x1) with each stream's MLP shift / scale
+  AdaLNArgs a2{B, N, H, x1, 1, (long long)N * H, 0, y, (long long)N * H, n_txt,
+               slot(kTxt, kShiftM), slot(kTxt, kScaleM), slot(kImg, kShiftM), slot(kImg, kScaleM), ms, c.eps};
+  DIT_CUDA(launch_adaln(a2, st));
+
+  // 6. act = silu(y Wg^T) * (y Wu^T) -> cat[:, :, H:H+F], per stream
+  for (int i = 0; i < 2; ++i) {
+    p[i] = blank_problem();
+    p[i].a = y; p[i].a_rows_total = N; p[i].lda = H; p[i].a_row0 = row0[i]; p[i].rows = rows[i];
+    p[i].w = (const bf16*)sw[i]->mlp_in; p[i].n = 2 * F; p[i].k = H; p[i].epi = kEpiSwiGLU;
+    p[i].out = cat; p[i].out_bstride = (long long)N * (H + F); p[i].ld_out = H + F; p[i].out_row0 = row0[i];
+    p[i].out_col0 = H;
+  }
+  DIT_CUDA(launch_gemm(p, 2, B, c.eps, dst, kClsGemmSwiGLU, st));
+
+  // 7. x = x1 + gate_m * (act mlp_out^T), per stream
+  const int gate_m[2] = {kTxt + kGateM, kImg + kGateM};
+  for (int i = 0; i < 2; ++i) {
+    p[i] = blank_problem();
+    p[i].a = cat + H; p[i].a_rows_total = N; p[i].lda = H + F; p[i].a_row0 = row0[i]; p[i].rows = rows[i];
+    p[i].w = (const bf16*)sw[i]->mlp_out; p[i].n = H; p[i].k = F; p[i].epi = kEpiResidual;
+    p[i].res_f32 = x1; p[i].out = x; p[i].out_bstride = (long long)N * H; p[i].ld_out = H; p[i].out_row0 = row0[i];
+    p[i].gate = mod + (long long)gate_m[i] * H; p[i].gate_stride = ms;
+  }
+  DIT_CUDA(launch_gemm(p, 2, B, c.eps, dst, kClsGemmDualMlpOut, st));
+  return DIT_OK;
+}
+
+dit_status run_single_block(const dit_weights* w, int layer, const dit_shape* s, bf16* x, const bf16* mod,
+                            const float* rope, void* ws, cudaStream_t st) {
+  const dit_config& c = w->cfg;
+  const dit_single_weights& sw = w->single[layer];
+  const int B = s->batch, N = s->n_txt + s->n_img + s->n_ref, H = c.hidden, F = c.mlp_hidden;
+  const Layout L = layout(c, *s);
+  bf16 *y = bat(ws, L.y), *q = bat(ws, L.q), *k = bat(ws, L.k), *v = bat(ws, L.v), *cat = bat(ws, L.cat);
+  DeviceStatus* dst = status_of(ws);
+  const long long ms = 17LL * H;
+  const bf16* sh = mod + (long long)(kSingle + 0) * H;
+  const bf16* sc = mod + (long long)(kSingle + 1) * H;
+
+  AdaLNArgs a1{B, N, H, x, 0, (long long)N * H, 0, y, (long long)N * H, 0, sh, sc, sh, sc, ms, c.eps};
+  DIT_CUDA(launch_adaln(a1, st));
+
+  GemmProblemHost p = blank_problem();
+  p.a = y; p.a_rows_total = N; p.lda = H; p.a_row0 = 0; p.rows = N;
+  p.w = (const bf16*)sw.qkv_mlp; p.n = 3 * H + 2 * F; p.k = H; p.epi = kEpiQKV;
+  p.n_qkv = 3 * H; p.hidden = H; p.q = q; p.kk = k; p.v = v;
+  p.q_norm = (const bf16*)sw.q_norm; p.k_norm = (const bf16*)sw.k_norm; p.rope = rope; p.seq = N; p.tok0 = 0;
+  p.out = cat; p.out_bstride = (long long)N * (H + F); p.ld_out = H + F; p.out_row0 = 0; p.out_col0 = H;
+  DIT_CUDA(launch_gemm(&p, 1, B, c.eps, dst, kClsGemmFused, st));
+
+  DIT_CUDA(launch_attention(B, c.heads, N, q, k, v, cat, H + F, dst, st));
+
+  p = blank_problem();
+  p.a = cat; p.a_rows_total = N; p.lda = H + F; p.a_row0 = 0; p.rows = N;
+  p.w = (const bf16*)sw.out; p.n = H; p.k = H + F; p.epi = kEpiResidual;
+  p.out = x; p.out_bstride = (long long)N * H; p.ld_out = H; p.out_row0 = 0;
+  p.gate = mod + (long long)(kSingle + 2) * H; p.gate_stride = ms;
+  DIT_CUDA(launch_gemm(&p, 1, B, c.eps, dst, kClsGemmSingleOut, st));
+  return DIT_OK;
+}
+
+dit_status run_modulation(const dit_weights* w, const float* sigma, int batch, bf16* mod, void* ws,
+                          const Layout& L, cudaStream_t st) {
+  const int H = w->cfg.hidden;
+  float* h1 = reinterpret_cast<float*>(at(ws, L.h1));
+  float* h2 = reinterpret_cast<float*>(at(ws, L.h2));
+  DIT_CUDA(launch_timestep_in((const bf16*)w->mod.t_in, H, 256, sigma, batch, h1, st));
+  DIT_CUDA(launch_gemv((const bf16*)w->mod.t_out, H, H, h1, batch, 1, h2, nullptr, st));
+  DIT_CUDA(launch_gemv((const bf16*)w->mod.mod, 17 * H, H, h2, batch, 0, nullptr, mod, st));
+  return DIT_OK;
+}
+
+dit_status check_step_weights(const dit_weights* w) {
+  if (!w) return DIT_ERR_INVALID_ARG;
+  DIT_TRY(check_config(&w->cfg));
+  if (!aligned16(w->mod.t_in) || !aligned16(w->mod.t_out) || !aligned16(w->mod.mod) || !aligned16(w->x_emb) ||
+      !aligned16(w->ctx_emb) || !aligned16(w->proj_out))
+    return DIT_ERR_INVALID_ARG;
+  if (w->cfg.n_dual > 0 && !w->dual) return DIT_ERR_INVALID_ARG;
+  if (w->cfg.n_single > 0 && !w->single) return DIT_ERR_INVALID_ARG;
+  for (int i = 0; i < w->cfg.n_dual; ++i) {
+    DIT_TRY(check_stream_weights(w->dual[i].img));
+    DIT_TRY(check_stream_weights(w->dual[i].txt));
+  }
+  for (int i = 0; i < w->cfg.n_single; ++i) {
+    const dit_single_weights& s = w->single[i];
+    if (!aligned16(s.qkv_mlp) || !aligned16(s.q_norm) || !aligned16(s.k_norm) || !aligned16(s.out))
+      return DIT_ERR_INVALID_ARG;
+  }
+  return DIT_OK;
+}
+
+dit_status run_step(const dit_weights* w, const dit_shape* s, const bf16* img, const bf16* ref, const bf16* txt,
+                    const float* rope, const float* sigma, bf16* vel, void* ws, cudaStream_t st) {
+  const dit_config& c = w->cfg;
+  const Layout L = layout(c, *s);
+  const int B = s->batch, N = s->n_txt + s->n_img + s->n_ref, H = c.hidden, C = c.in_channels;
+  bf16* mod = bat(ws, L.mod);
+  bf16* x = bat(ws, L.x);
+  bf16* y = bat(ws, L.y);
+  DeviceStatus* dst = status_of(ws);
+
+  DIT_TRY(run_modulation(w, sigma, B, mod, ws, L, st));
+
+  // Embedders: text rows by ctx_emb, target-image rows by x_emb, into one [B, N, H].
+  GemmProblemHost p[2];
+  p[0] = blank_problem();
+  p[0].a = txt; p[0].a_rows_total = s->n_txt; p[0].lda = c.txt_dim; p[0].rows = s->n_txt;
+  p[0].w = (const bf16*)w->ctx_emb; p[0].n = H; p[0].k = c.txt_dim; p[0].epi = kEpiStore;
+  p[0].out = x; p[0].out_bstride = (long long)N * H; p[0].ld_out = H; p[0].out_row0 = 0;
+  p[1] = blank_problem();
+  p[1].a = img; p[1].a_rows_total = s->n_img; p[1].lda = C; p[1].rows = s->n_img;
+  p[1].w = (const bf16*)w->x_emb; p[1].n = H; p[1].k = C; p[1].epi = kEpiStore;
+  p[1].out = x; p[1].out_bstride = (long long)N * H; p[1].ld_out = H; p[1].out_row0 = s->n_txt;
+  DIT_CUDA(launch_gemm(p, 2, B, c.eps, dst, kClsGemmPlain, st));
+  if (s->n_ref > 0) {
+    p[0] = blank_problem();
+    p[0].a = ref; p[0].a_rows_total = s->n_ref; p[0].lda = C; p[0].rows = s->n_ref;
+    p[0].w = (const bf16*)w->x_emb; p[0].n = H; p[0].k = C; p[0].epi = kEpiStore;
+    p[0].out = x; p[0].out_bstride = (long long)N * H; p[0].ld_out = H; p[0].out_row0 = s->n_txt + s->n_img;
+    DIT_CUDA(launch_gemm(p, 1, B, c.eps, dst, kClsGemmPlain, st));
+  }
+
+  for (int i = 0; i < c.n_dual; ++i) DIT_TRY(run_dual_block(w, i, s, x, mod, rope, ws, st));
+  for (int i = 0; i < c.n_single; ++i) DIT_TRY(run_single_block(w, i, s, x, mod, rope, ws, st));
+
+  // Final layer on the target-image rows only.
+  const long long ms = 17LL * H;
+  const bf16* fsh = mod + (long long)(kFinal + 0) * H;
+  const bf16* fsc = mod + (long long)(kFinal + 1) * H;
+  AdaLNArgs af{B, s->n_img, H, x, 0, (long long)N * H, s->n_txt, y, (long long)s->n_img * H, 0, fsh, fsc, fsh, fsc, ms,
+               c.eps};
+  DIT_CUDA(launch_adaln(af, st));
+  p[0] = blank_problem();
+  p[0].a = y; p[0].a_rows_total = s->n_img; p[0].lda = H; p[0].rows = s->n_img;
+  p[0].w = (const bf16*)w->proj_out; p[0].n = C; p[0].k = H; p[0].epi = kEpiStore;
+  p[0].out = vel; p[0].out_bstride = (long long)s->n_img * C; p[0].ld_out = C; p[0].out_row0 = 0;
+  DIT_CUDA(launch_gemm(p, 1, B, c.eps, dst, kClsGemmPlain, st));
+  return DIT_OK;
+}
+
+}  // namespace
+}  // namespace dit
+
+using namespace dit;
+
+// ---------------------------------------------------------------------------------
+// C ABI
+// ---------------------------------------------------------------------------------
+extern "C" {
+
+const char* dit_status_string(dit_status s) {
+  switch (s) {
+    case DIT_OK: return "ok";
+    case DIT_ERR_INVALID_ARG: return "invalid argument";
+    case DIT_ERR_UNSUPPORTED: return "unsupported configuration";
+    case DIT_ERR_WORKSPACE: return "workspace too small";
+    case DIT_ERR_CUDA: return "CUDA error";
+    case DIT_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+dit_status dit_config_klein(dit_config* cfg) {
+  if (!cfg) return DIT_ERR_INVALID_ARG;
+  cfg->hidden = 3072;
+  cfg->heads = 24;
+  cfg->head_dim = 128;
+  cfg->mlp_hidden = 9216;
+  cfg->n_dual = 5;
+  cfg->n_single = 20;
+  cfg->in_channels = 128;
+  cfg->txt_dim = 7680;
+  cfg->rope_theta = 2000.0f;
+  for (int i = 0; i < 4; ++i) cfg->axes_dim[i] = 32;
+  cfg->eps = 1e-6f;
+  return DIT_OK;
+}
+
+dit_status dit_workspace_size(const dit_config* cfg, const dit_shape* shape, size_t* bytes) {
+  DIT_TRY(check_config(cfg));
+  DIT_TRY(check_shape(shape));
+  if (!bytes) return DIT_ERR_INVALID_ARG;
+  *bytes = layout(*cfg, *shape).total;
+  return DIT_OK;
+}
+
+dit_status dit_token_ids(const dit_shape* shape, int grid_h, int grid_w, const int* ref_grids_host, int n_refs,
+                         int32_t* ids_host) {
+  DIT_TRY(check_shape(shape));
+  if (!ids_host || grid_h < 1 || grid_w < 1 || n_refs < 0 || (n_refs > 0 && !ref_grids_host))
+    return DIT_ERR_INVALID_ARG;
+  if ((long long)grid_h * grid_w != shape->n_img) return DIT_ERR_INVALID_ARG;
+  long long nref = 0;
+  for (int i = 0; i < n_refs; ++i) {
+    if (ref_grids_host[2 * i] < 1 || ref_grids_host[2 * i + 1] < 1) return DIT_ERR_INVALID_ARG;
+    nref += (long long)ref_grids_host[2 * i] * ref_grids_host[2 * i + 1];
+  }
+  if (nref != shape->n_ref) return DIT_ERR_INVALID_ARG;
+  int32_t* o = ids_host;
+  auto put = [&](int t, int h, int w, int l) {
+    o[0] = t;
+    o[1] = h;
+    o[2] = w;
+    o[3] = l;
+    o += 4;
+  };
+  for (int i = 0; i < shape->n_txt; ++i) put(0, 0, 0, i);
+  for (int r = 0; r < grid_h; ++r)
+    for (int c = 0; c < grid_w; ++c) put(0, r, c, 0);
+  for (int i = 0; i < n_refs; ++i)
+    for (int r = 0; r < ref_grids_host[2 * i]; ++r)
+      for (int c = 0; c < ref_grids_host[2 * i + 1]; ++c) put(10 + 10 * i, r, c, 0);
+  return DIT_OK;
+}
+
+dit_status dit_rope_table(const dit_config* cfg, const int32_t* ids_dev, int n, float* table_dev,
+                          dit_stream_t stream) {
+  DIT_TRY(check_config(cfg));
+  if (n < 0 || n > kMaxTokens) return DIT_ERR_INVALID_ARG;
+  if (n == 0) return DIT_OK;
+  if (!aligned16(ids_dev) || !aligned16(table_dev)) return DIT_ERR_INVALID_ARG;
+  return cuda_status(launch_rope_table(ids_dev, n, cfg->axes_dim, cfg->rope_theta, table_dev, (cudaStream_t)stream));
+}
+
+dit_status dit_pack_mlp_in(const void* src_dev, void* dst_dev, int mlp_hidden, int cols, dit_stream_t stream) {
+  if (!aligned16(src_dev) || !aligned16(dst_dev)) return DIT_ERR_INVALID_ARG;
+  if (mlp_hidden <= 0 || mlp_hidden % 128 != 0 || cols <= 0 || cols % 8 != 0) return DIT_ERR_INVALID_ARG;
+  const uintptr_t a = (uintptr_t)src_dev, b = (uintptr_t)dst_dev, len = (uintptr_t)2 * mlp_hidden * cols * 2;
+  if (a < b + len && b < a + len) return DIT_ERR_INVALID_ARG;
+  return cuda_status(launch_pack_mlp_in((const bf16*)src_dev, (bf16*)dst_dev, mlp_hidden, cols, (cudaStream_t)stream));
+}
+
+dit_status dit_modulation(const dit_weights* w, const float* sigma_dev, int batch, void* mod_dev, void* ws,
+                          size_t ws_bytes, dit_stream_t stream) {
+  if (!w) return DIT_ERR_INVALID_ARG;
+  DIT_TRY(check_config(&w->cfg));
+  if (batch < 1 || batch > kMaxBatch) return DIT_ERR_INVALID_ARG;
+  if (!aligned16(w->mod.t_in) || !aligned16(w->mod.t_out) || !aligned16(w->mod.mod)) return DIT_ERR_INVALID_ARG;
+  if (!aligned16(sigma_dev) || !aligned16(mod_dev) || !aligned16(ws)) return DIT_ERR_INVALID_ARG;
+  const dit_shape s{batch, 1, 1, 0};
+  const Layout L = layout(w->cfg, s);
+  if (ws_bytes < L.h2 + (size_t)batch * w->cfg.hidden * 4) return DIT_ERR_WORKSPACE;
+  return run_modulation(w, sigma_dev, batch, (bf16*)mod_dev, ws, L, (cudaStream_t)stream);
+}
+
+dit_status dit_dual_block_fwd(const dit_weights* w, int layer, const dit_shape* shape, void* x_dev,
+                              const void* mod_dev, const float* rope_dev, void* ws, size_t ws_bytes,
+                              dit_stream_t stream) {
+  DIT_TRY(check_block_args(w, shape, x_dev, mod_dev, rope_dev, ws, ws_bytes));
+  if (layer < 0 || layer >= w->cfg.n_dual || !w->dual) return DIT_ERR_INVALID_ARG;
+  DIT_TRY(check_stream_weights(w->dual[layer].img));
+  DIT_TRY(check_stream_weights(w->dual[layer].txt));
+  return run_dual_block(w, layer, shape, (bf16*)x_dev, (const bf16*)mod_dev, rope_dev, ws, (cudaStream_t)stream);
+}
+
+dit_status dit_single_block_fwd(const dit_weights* w, int layer, const dit_shape* shape, void* x_dev,
+                                const void* mod_dev, const float* rope_dev, void* ws, size_t ws_bytes,
+                                dit_stream_t stream) {
+  DIT_TRY(check_block_args(w, shape, x_dev, mod_dev, rope_dev, ws, ws_bytes));
+  if (layer < 0 || layer >= w->cfg.n_single || !w->single) return DIT_ERR_INVALID_ARG;
+  const dit_single_weights& s = w->single[layer];
+  if (!aligned16(s.qkv_mlp) || !aligned16(s.q_norm) || !aligned16(s.k_norm) || !aligned16(s.out))
+    return DIT_ERR_INVALID_ARG;
+  return run_single_block(w, layer, shape, (bf16*)x_dev, (const bf16*)mod_dev, rope_dev, ws, (cudaStream_t)stream);
+}
+
+dit_status dit_step_fwd(const dit_weights* w, const dit_shape* shape, const void* img_tokens,
+                        const void* ref_tokens, const void* txt_emb, const float* rope_dev, const float* sigma_dev,
+                        void* velocity_out, void* ws, size_t ws_bytes, dit_stream_t stream) {
+  DIT_TRY(check_step_weights(w));
+  DIT_TRY(check_shape(shape));
+  if (!aligned16(img_tokens) || !aligned16(txt_emb) || !aligned16(rope_dev) || !aligned16(sigma_dev) ||
+      !aligned16(velocity_out) || !aligned16(ws))
+    return DIT_ERR_INVALID_ARG;
+  if ((shape->n_ref > 0) != (ref_tokens != nullptr)) return DIT_ERR_INVALID_ARG;
+  if (ref_tokens && !aligned16(ref_tokens)) return DIT_ERR_INVALID_ARG;
+  if (ws_bytes < layout(w->cfg, *shape).step_end) return DIT_ERR_WORKSPACE;
+  return run_step(w, shape, (const bf16*)img_tokens, (const bf16*)ref_tokens, (const bf16*)txt_emb, rope_dev,
+                  sigma_dev, (bf16*)velocity_out, ws, (cudaStream_t)stream);
+}
+
+dit_status dit_step_host(const dit_weights* w, const dit_shape* shape, const void* img_tokens_host,
+                         const void* ref_tokens_host, const void* txt_emb_host, const float* rope_dev,
+                         const float* sigma_host, void* velocity_host, void* ws, size_t ws_bytes,
+                         dit_stream_t stream) {
+  DIT_TRY(check_step_weights(w));
+  DIT_TRY(check_shape(shape));
+  if (!img_tokens_host || !txt_emb_host || !sigma_host || !velocity_host || !aligned16(rope_dev) || !aligned16(ws))
+    return DIT_ERR_INVALID_ARG;
+  if ((shape->n_ref > 0) != (ref_tokens_host != nullptr)) return DIT_ERR_INVALID_ARG;
+  const Layout L = layout(w->cfg, *shape);
+  if (ws_bytes < L.total) return DIT_ERR_WORKSPACE;
+  const cudaStream_t st = (cudaStream_t)stream;
+  const size_t B = shape->batch, C = w->cfg.in_channels;
+  const size_t img_b = B * shape->n_img * C * 2, ref_b = B * shape->n_ref * C * 2,
+               txt_b = B * shape->n_txt * (size_t)w->cfg.txt_dim * 2;
+  DIT_CUDA(cudaMemcpyAsync(at(ws, L.in_img), img_tokens_host, img_b, cudaMemcpyHostToDevice, st));
+  if (ref_b) DIT_CUDA(cudaMemcpyAsync(at(ws, L.in_ref), ref_tokens_host, ref_b, cudaMemcpyHostToDevice, st));
+  DIT_CUDA(cudaMemcpyAsync(at(ws, L.in_txt), txt_emb_host, txt_b, cudaMemcpyHostToDevice, st));
+  DIT_CUDA(cudaMemcpyAsync(at(ws, L.in_sigma), sigma_host, B * 4, cudaMemcpyHostToDevice, st));
+  DIT_TRY(run_step(w, shape, bat(ws, L.in_img), ref_b ? bat(ws, L.in_ref) : nullptr, bat(ws, L.in_txt), rope_dev,
+                   reinterpret_cast<const float*>(at(ws, L.in_sigma)), bat(ws, L.out_vel), ws, st));
+  DIT_CUDA(cudaMemcpyAsync(velocity_host, at(ws, L.out_vel), img_b, cudaMemcpyDeviceToHost, st));
+  return DIT_OK;
+}
+
+dit_status dit_sync_status(void* ws, dit_stream_t stream, uint32_t* where_out) {
+  if (!aligned16(ws)) return DIT_ERR_INVALID_ARG;
+  const cudaStream_t st = (cudaStream_t)stream;
+  DeviceStatus h;
+  DIT_CUDA(cudaMemcpyAsync(&h, ws, 8, cudaMemcpyDeviceToHost, st));
+  DIT_CUDA(cudaStreamSynchronize(st));
+  if (where_out) *where_out = h.where;
+  if (h.word != 0) {
+    DIT_CUDA(cudaMemsetAsync(ws, 0, 8, st));
+    DIT_CUDA(cudaStreamSynchronize(st));
+    return DIT_ERR_TIMEOUT;
+  }
+  return DIT_OK;
+}
+
+dit_status dit_adaln(int batch, int rows, int hidden, const void* x_dev, int x_rows, int x_row0, int split,
+                     const void* shift_lo, const void* scale_lo, const void* shift_hi, const void* scale_hi,
+                     long long mod_stride, float eps, void* y_dev, dit_stream_t stream) {
+  if (batch < 1 || rows < 0 || x_rows < 0 || x_row0 < 0 || (long long)x_row0 + rows > x_rows) return DIT_ERR_INVALID_ARG;
+  if (!adaln_supports(hidden)) return DIT_ERR_UNSUPPORTED;
+  if (!aligned16(x_dev) || !aligned16(y_dev) || !aligned16(shift_lo) || !aligned16(scale_lo) ||
+      !aligned16(shift_hi) || !aligned16(scale_hi) || mod_stride < 0 || mod_stride % 8 != 0 || !(eps > 0.f))
+    return DIT_ERR_INVALID_ARG;
+  AdaLNArgs a{batch, rows, hidden, x_dev, 0, (long long)x_rows * hidden, x_row0, (bf16*)y_dev,
+              (long long)rows * hidden, split, (const bf16*)shift_lo, (const bf16*)scale_lo, (const bf16*)shift_hi,
+              (const bf16*)scale_hi, mod_stride, eps};
+  return cuda_status(launch_adaln(a, (cudaStream_t)stream));
+}
+
+dit_status dit_linear(int batch, int rows, int n_out, int k, const void* a_dev, const void* w_dev, void* out_dev,
+                      int ld_out, dit_epilogue epi, const void* gate_dev, long long gate_stride, void* ws,
+                      size_t ws_bytes, dit_stream_t stream) {
+  if (batch < 1 || batch > kMaxBatch || rows < 1 || n_out < 1 || k < 1 || k % 8 != 0 || n_out % 32 != 0 ||
+      ld_out < n_out || ld_out % 8 != 0)
+    return DIT_ERR_INVALID_ARG;
+  if (!aligned16(a_dev) || !aligned16(w_dev) || !aligned16(out_dev) || !aligned16(ws)) return DIT_ERR_INVALID_ARG;
+  if (ws_bytes < sizeof(DeviceStatus)) return DIT_ERR_WORKSPACE;
+  GemmProblemHost p = blank_problem();
+  p.a = (const bf16*)a_dev; p.a_rows_total = rows; p.lda = k; p.rows = rows;
+  p.w = (const bf16*)w_dev; p.n = n_out; p.k = k;
+  p.out = (bf16*)out_dev; p.out_bstride = (long long)rows * ld_out; p.ld_out = ld_out;
+  int cls = kClsGemmPlain;
+  switch (epi) {
+    case DIT_EPI_STORE: p.epi = kEpiStore; break;
+    case DIT_EPI_GATED_RESIDUAL:
+      if (!aligned16(gate_dev) || gate_stride < 0 || gate_stride % 8 != 0) return DIT_ERR_INVALID_ARG;
+      p.epi = kEpiResidual; p.gate = (const bf16*)gate_dev; p.gate_stride = gate_stride; cls = kClsGemmResidual;
+      break;
+    case DIT_EPI_SWIGLU:
+      if (n_out % 128 != 0) return DIT_ERR_INVALID_ARG;
+      p.epi = kEpiSwiGLU; p.n = 2 * n_out; cls = kClsGemmSwiGLU;
+      break;
+    default: return DIT_ERR_INVALID_ARG;
+  }
+  return cuda_status(launch_gemm(&p, 1, batch, 1e-6f, status_of(ws), cls, (cudaStream_t)stream));
+}
+
+dit_status dit_attention(int batch, int heads, int n, const void* q_dev, const void* k_dev, const void* v_dev,
+                         void* out_dev, int ld_out, void* ws, size_t ws_bytes, dit_stream_t stream) {
+  if (batch < 1 || batch > kMaxBatch || heads < 1 || n < 1 || n > kMaxTokens || ld_out < 128 * heads ||
+      ld_out % 8 != 0)
+    return DIT_ERR_INVALID_ARG;
+  if (!aligned16(q_dev) || !aligned16(k_dev) || !aligned16(v_dev) || !aligned16(out_dev) || !aligned16(ws))
+    return DIT_ERR_INVALID_ARG;
+  if (ws_bytes < sizeof(DeviceStatus)) return DIT_ERR_WORKSPACE;
+  return cuda_status(launch_attention(batch, heads, n, (const bf16*)q_dev, (const bf16*)k_dev, (const bf16*)v_dev,
+                                      (bf16*)out_dev, ld_out, status_of(ws), (cudaStream_t)stream));
+}
+
+unsigned long long dit_launch_count(void) { return g_launches.load(); }
+
+dit_status dit_timing_begin(int max_records) {
+  if (max_records < 1 || max_records > (1 << 20)) return DIT_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_timing_mu);
+  for (auto& r : g_recs) {
+    cudaEventDestroy(r.start);
+    cudaEventDestroy(r.stop);
+  }
+  g_recs.clear();
+  g_recs.resize(max_records);
+  for (auto& r : g_recs) {
+    r.cls = -1;
+    if (cudaEventCreate(&r.start) != cudaSuccess || cudaEventCreate(&r.stop) != cudaSuccess) {
+      g_recs.clear();
+      return DIT_ERR_CUDA;
+    }
+  }
+  g_rec_used = 0;
+  g_timing_on = true;
+  return DIT_OK;
+}
+
+dit_status dit_timing_end(int* n, int* classes, float* ms, int cap) {
+  if (!n || cap < 0 || (cap > 0 && (!classes || !ms))) return DIT_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_timing_mu);
+  g_timing_on = false;
+  const int used = g_rec_used < cap ? g_rec_used : cap;
+  for (int i = 0; i < used; ++i) {
+    if (cudaEventSynchronize(g_recs[i].stop) != cudaSuccess) return DIT_ERR_CUDA;
+    float t = 0.f;
+    if (cudaEventElapsedTime(&t, g_recs[i].start, g_recs[i].stop) != cudaSuccess) return DIT_ERR_CUDA;
+    classes[i] = g_recs[i].cls;
+    ms[i] = t;
+  }
+  *n = used;
+  return DIT_OK;
+}
+
+const char* dit_kernel_class_name(int cls) { return kernel_class_name(cls); }
+
+}  // extern "C"

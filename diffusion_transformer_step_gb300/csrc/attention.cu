@@ -1,0 +1,359 @@
+// Joint text + image attention on the tensor cores: O = softmax(Q K^T / sqrt(128)) V over
+// every key of the joint sequence, no mask ("flux2-klein-p100a" Caveats: all 512 padded
+// text rows enter with no mask; reading R6 for the scale).  Padded tail keys of a tile
+// (sequence length not a multiple of 128) are masked out, padded tail queries not stored.
+//
+// One CTA per (128-query tile, head, batch row), 192 threads:
+//   warp 0      TMA: Q once; K_j and V_j tiles (128 keys x 128 dims, two 64-dim halves,
+//               128-byte swizzle) into a 2-stage ring, separate full/empty barriers for
+//               K and V so K_{j+2} streams in as soon as S_j is computed;
+//   warp 1      tcgen05.mma from one thread: S_j = Q K_j^T into one of two 128-column
+//               TMEM buffers, then O += P_{j-1} V_{j-1} (A = P from shared memory,
+//               K-major; B = V, MN-major) into a 128-column TMEM accumulator;
+//   warps 2-5   online softmax, one thread per query row: S row from TMEM, exp2 with
+//               the log2(e)/sqrt(d) scale folded in, P rounded to bf16 into shared memory
+//               (128-byte swizzled, the layout a TMA load would produce), O rescaled in
+//               TMEM only when the running maximum grows by more than 2^8 (the stale
+//               maximum keeps every P <= 256, exact after the final 1/l).
+// TMEM: S0 [0,128), S1 [128,256), O [256,384) of a 512-column allocation.
+#include <math.h>
+
+#include "runtime.h"
+
+namespace dit {
+
+namespace {
+
+constexpr int kBQ = 128, kBKV = 128;
+constexpr int kThreads = 192;
+constexpr uint32_t kHalfBytes = 128 * 64 * 2;   // one 64-dim half of a 128-row tile
+constexpr uint32_t kTileBytes = 2 * kHalfBytes;  // 32 KB
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffK = kOffQ + kTileBytes;
+constexpr uint32_t kOffV = kOffK + 2 * kTileBytes;
+constexpr uint32_t kOffP = kOffV + 2 * kTileBytes;
+constexpr uint32_t kOffBar = kOffP + kTileBytes;
+constexpr size_t kSmemBytes = 1024 + kOffBar + 256;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+struct alignas(64) AttnParams {
+  CUtensorMap q_map, k_map, v_map;
+  bf16* out;
+  int ld_out, n, heads;
+  float scale_log2;
+  DeviceStatus* status;
+};
+
+enum : uint32_t {
+  kSiteQ = 0x201, kSiteKEmpty, kSiteVEmpty, kSiteKFull, kSiteSFree, kSitePFull, kSiteVFull, kSiteSFull, kSiteODone
+};
+
+__global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_constant__ AttnParams P) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* q_full = bars + 0;
+  uint64_t* k_full = bars + 1;   // [2]
+  uint64_t* k_empty = bars + 3;  // [2]
+  uint64_t* v_full = bars + 5;   // [2]
+  uint64_t* v_empty = bars + 7;  // [2]
+  uint64_t* s_full = bars + 9;   // [2]
+  uint64_t* s_free = bars + 11;  // [2]
+  uint64_t* p_full = bars + 13;
+  uint64_t* o_done = bars + 14;
+  uint64_t* drain = bars + 15;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n = P.n;
+  const int nkv = (n + kBKV - 1) / kBKV;
+  const int q0 = blockIdx.x * kBQ;
+  const int head = blockIdx.y, b = blockIdx.z;
+  const int bh = b * P.heads + head;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], 4);
+    }
+    mbar_init(p_full, 4);
+    mbar_init(o_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&P.q_map);
+    tma_prefetch_desc(&P.k_map);
+    tma_prefetch_desc(&P.v_map);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtx wc{P.status, abort_flag, kWaitLimitNs};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int pending_k = 0, pending_v = 0;  // loads issued whose completion was not observed
+      bool ok = true;
+      mbar_arrive_expect_tx(q_full, kTileBytes);
+      tma_load_3d(smem + kOffQ, &P.q_map, q_full, 0, q0, bh);
+      tma_load_3d(smem + kOffQ + kHalfBytes, &P.q_map, q_full, 64, q0, bh);
+      for (int j = 0; j < nkv && ok; ++j) {
+        const int st = j & 1;
+        const uint32_t ph = (uint32_t)(j >> 1) & 1u;
+        if (!mbar_wait(&k_empty[st], ph ^ 1u, wc, kSiteKEmpty)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&k_full[st], kTileBytes);
+        tma_load_3d(smem + kOffK + st * kTileBytes, &P.k_map, &k_full[st], 0, j * kBKV, bh);
+        tma_load_3d(smem + kOffK + st * kTileBytes + kHalfBytes, &P.k_map, &k_full[st], 64, j * kBKV, bh);
+        pending_k = j + 1;
+        if (!mbar_wait(&v_empty[st], ph ^ 1u, wc, kSiteVEmpty)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&v_full[st], kTileBytes);
+        tma_load_3d(smem + kOffV + st * kTileBytes, &P.v_map, &v_full[st], 0, j * kBKV, bh);
+        tma_load_3d(smem + kOffV + st * kTileBytes + kHalfBytes, &P.v_map, &v_full[st], 64, j * kBKV, bh);
+        pending_v = j + 1;
+      }
+      if (!ok) {
+        // Unwinding: let copies in flight land (bounded) before the block exits.
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try(q_full, 0) && global_timer_ns() - t0 < 100000000ull) {
+        }
+        for (int j = (pending_k > 2 ? pending_k - 2 : 0); j < pending_k; ++j)
+          while (!mbar_try(&k_full[j & 1], (uint32_t)(j >> 1) & 1u) && global_timer_ns() - t0 < 200000000ull) {
+          }
+        for (int j = (pending_v > 2 ? pending_v - 2 : 0); j < pending_v; ++j)
+          while (!mbar_try(&v_full[j & 1], (uint32_t)(j >> 1) & 1u) && global_timer_ns() - t0 < 300000000ull) {
+          }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_qk = make_idesc_bf16(128, 128, false);
+      const uint32_t idesc_pv = make_idesc_bf16(128, 128, true);
+      const uint32_t sQ = smem_u32(smem + kOffQ);
+      const uint32_t sP = smem_u32(smem + kOffP);
+      const uint32_t tO = tmem + 256;
+      bool ok = mbar_wait(q_full, 0, wc, kSiteQ);
+      auto issue_pv = [&](int i) -> bool {
+        const int st = i & 1;
+        if (!mbar_wait(p_full, (uint32_t)i & 1u, wc, kSitePFull)) return false;
+        if (!mbar_wait(&v_full[st], (uint32_t)(i >> 1) & 1u, wc, kSiteVFull)) return false;
+        tc_fence_after();
+        const uint32_t sV = smem_u32(smem + kOffV + st * kTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t ad = make_sdesc_sw128(sP + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = make_sdesc_sw128(sV + kk * 2048, kHalfBytes, 1024);
+          umma_bf16(tO, ad, bd, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(o_done);
+        umma_commit(&v_empty[st]);
+        return true;
+      };
+      for (int j = 0; j < nkv && ok; ++j) {
+        const int st = j & 1, sb = j & 1;
+        const uint32_t ph = (uint32_t)(j >> 1) & 1u;
+        if (!mbar_wait(&k_full[st], ph, wc, kSiteKFull) || !mbar_wait(&s_free[sb], ph ^ 1u, wc, kSiteSFree)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sK = smem_u32(smem + kOffK + st * kTileBytes);
+        const uint32_t tS = tmem + (uint32_t)(sb * 128);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t ad = make_sdesc_sw128(sQ + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = make_sdesc_sw128(sK + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
+          umma_bf16(tS, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&s_full[sb]);
+        umma_commit(&k_empty[st]);
+        if (j > 0 && !issue_pv(j - 1)) ok = false;
+      }
+      if (ok) issue_pv(nkv - 1);
+      umma_commit(drain);
+      const uint64_t t0 = global_timer_ns();
+      while (!mbar_try(drain, 0) && global_timer_ns() - t0 < 1000000000ull) {
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax / correction / output
+    const int qq = warp & 3;
+    const int row = qq * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(qq * 32) << 16;
+    const uint32_t tO = tmem + 256 + lane_off;
+    uint8_t* sP = smem + kOffP;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nkv; ++j) {
+      const int sb = j & 1;
+      ok = mbar_wait(&s_full[sb], (uint32_t)(j >> 1) & 1u, wc, kSiteSFull);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      float s[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_load32(tmem + (uint32_t)(sb * 128 + c * 32) + lane_off, r);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[i]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free[sb]);
+
+      const int kv_valid = n - j * kBKV;
+      if (kv_valid < kBKV) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i)
+          if (i >= kv_valid) s[i] = -INFINITY;
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 128; ++i) mx = fmaxf(mx, s[i]);
+      const float m_cand = fmaxf(m_run, mx * P.scale_log2);
+      float alpha = 1.0f;
+      bool resc = false;
+      if (j == 0) {
+        m_run = m_cand;
+      } else if (m_cand > m_run + kRescaleThreshold) {
+        alpha = exp2f(m_run - m_cand);
+        m_run = m_cand;
+        resc = true;
+      }
+      float psum = 0.f;
+#pragma unroll
+      for (int i = 0; i < 128; ++i) {
+        s[i] = exp2f(fmaf(s[i], P.scale_log2, -m_run));
+        psum += s[i];
+      }
+      l_run = l_run * alpha + psum;
+
+      if (j > 0) {
+        bool ok2 = mbar_wait(o_done, (uint32_t)(j - 1) & 1u, wc, kSiteODone);
+        ok2 = __all_sync(0xffffffffu, ok2);
+        if (!ok2) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t r[32];
+            tmem_load32(tO + c * 32, r);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+            tmem_store32(tO + c * 32, r);
+          }
+          tmem_store_wait();
+        }
+      }
+      // P (bf16) into the 128-byte-swizzled K-major layout: half h holds keys
+      // [64h, 64h + 64); row r's 16-byte chunk c sits at chunk position c ^ (r & 7).
+#pragma unroll
+      for (int c8 = 0; c8 < 16; ++c8) {
+        const int half = c8 >> 3, chunk = c8 & 7;
+        uint4 v;
+        v.x = pack_bf16x2(s[c8 * 8 + 0], s[c8 * 8 + 1]);
+        v.y = pack_bf16x2(s[c8 * 8 + 2], s[c8 * 8 + 3]);
+        v.z = pack_bf16x2(s[c8 * 8 + 4], s[c8 * 8 + 5]);
+        v.w = pack_bf16x2(s[c8 * 8 + 6], s[c8 * 8 + 7]);
+        *reinterpret_cast<uint4*>(sP + half * kHalfBytes + row * 128 + ((chunk ^ (row & 7)) << 4)) = v;
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
+    }
+    if (ok) {
+      bool ok2 = mbar_wait(o_done, (uint32_t)(nkv - 1) & 1u, wc, kSiteODone);
+      ok2 = __all_sync(0xffffffffu, ok2);
+      if (ok2) {
+        tc_fence_after();
+        const int tok = q0 + row;
+        const float inv_l = 1.0f / l_run;
+        bf16* dst = P.out + ((long long)b * n + tok) * P.ld_out + head * 128;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tmem_load32(tO + c * 32, r);
+          if (tok < n) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              d4[i] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * i + 0]) * inv_l, __uint_as_float(r[8 * i + 1]) * inv_l),
+                                 pack_bf16x2(__uint_as_float(r[8 * i + 2]) * inv_l, __uint_as_float(r[8 * i + 3]) * inv_l),
+                                 pack_bf16x2(__uint_as_float(r[8 * i + 4]) * inv_l, __uint_as_float(r[8 * i + 5]) * inv_l),
+                                 pack_bf16x2(__uint_as_float(r[8 * i + 6]) * inv_l, __uint_as_float(r[8 * i + 7]) * inv_l));
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+bool g_attr_set[16] = {false};
+
+}  // namespace
+
+cudaError_t launch_attention(int batch, int heads, int n, const bf16* q, const bf16* k, const bf16* v, bf16* out,
+                             int ld_out, DeviceStatus* status, cudaStream_t s) {
+  if (batch <= 0 || heads <= 0 || n <= 0) return cudaSuccess;
+  AttnParams P;
+  memset(&P, 0, sizeof(P));
+  const uint64_t dims[3] = {128, (uint64_t)n, (uint64_t)batch * heads};
+  const uint64_t str[2] = {256, (uint64_t)n * 256};
+  const uint32_t box[3] = {64, 128, 1};
+  if (!encode_tmap_bf16(&P.q_map, q, 3, dims, str, box)) return cudaErrorInvalidValue;
+  if (!encode_tmap_bf16(&P.k_map, k, 3, dims, str, box)) return cudaErrorInvalidValue;
+  if (!encode_tmap_bf16(&P.v_map, v, 3, dims, str, box)) return cudaErrorInvalidValue;
+  P.out = out;
+  P.ld_out = ld_out;
+  P.n = n;
+  P.heads = heads;
+  P.scale_log2 = (float)(1.4426950408889634 / sqrt(128.0));
+  P.status = status;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 16 && !g_attr_set[dev]) {
+    cudaError_t e =
+        cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    g_attr_set[dev] = true;
+  }
+  dim3 grid((n + kBQ - 1) / kBQ, heads, batch);
+  LaunchScope scope(kClsAttention, s);
+  attention_kernel<<<grid, kThreads, kSmemBytes, s>>>(P);
+  return cudaGetLastError();
+}
+
+}  // namespace dit

@@ -1,0 +1,476 @@
+// Persistent tcgen05 GEMM with fused epilogues: out = A W^T, A [rows, k] and W [n, k]
+// both K-major bf16, fp32 accumulation in Tensor Memory.
+//
+// One CTA per SM, 192 threads:
+//   warp 0      TMA producer: A tile 128 x 64 and W tile 256 x 64 per stage, 128-byte
+//               swizzle, 4-stage shared-memory ring guarded by full/empty mbarriers;
+//   warp 1      allocates 512 TMEM columns (two 128 x 256 fp32 accumulators) and issues
+//               tcgen05.mma (M=128, N=256, K=16) from one thread, committing each stage
+//               back to its empty barrier and each finished tile to an accumulator-full
+//               barrier;
+//   warps 2-5   epilogue: one thread per accumulator row, tcgen05.ld 32 columns at a
+//               time, fused math, 16-byte global stores; then hand the accumulator back.
+// The two accumulators let tile i's epilogue overlap tile i+1's main loop.  Up to two
+// problems (the text and image streams of a dual-stream block) share one launch; tiles
+// are ordered with M fastest so that concurrent CTAs share the same weight slab in L2.
+//
+// Epilogues (the fused block maths):
+//   STORE     bf16(acc)
+//   RESIDUAL  out <- x + gate * acc  (gated residual, reading R4); x and out bf16 or
+//             fp32, possibly the same buffer
+//   SWIGLU    silu(acc[gate cols]) * acc[up cols]          (reading R9; packed W rows)
+//   QKV       columns [0, 3H): per-head RMSNorm (fp32, eps) * w, RoPE on adjacent pairs
+//             from the fp32 table, written head-major [B, heads, seq, 128]; columns
+//             >= 3H: SWIGLU into the concat buffer (single-stream fused projection).
+#include "runtime.h"
+
+namespace dit {
+
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int kStages = 4;
+constexpr int kThreads = 192;
+constexpr uint32_t kATileBytes = BM * BK * 2;  // 16 KB
+constexpr uint32_t kBTileBytes = BN * BK * 2;  // 32 KB
+constexpr uint32_t kStageBytes = kATileBytes + kBTileBytes;
+constexpr uint32_t kTmemCols = 2 * BN;
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + 256;
+
+struct DevProblem {
+  int rows, a_row0, n, k, m_tiles, n_tiles, tile_begin, epi;
+  bf16* out;
+  float* out_f32;
+  const bf16* res;
+  const float* res_f32;
+  long long out_bstride;
+  int ld_out, out_row0, out_col0;
+  const bf16* gate;
+  long long gate_stride;
+  int n_qkv, hidden;
+  bf16 *q, *kk, *v;
+  const bf16 *q_norm, *k_norm;
+  const float* rope;
+  int seq, tok0;
+};
+
+struct alignas(64) GemmParams {
+  CUtensorMap a_map[2];
+  CUtensorMap b_map[2];
+  DevProblem prob[2];
+  int nprob, batch, total_tiles;
+  float eps;
+  DeviceStatus* status;
+};
+
+struct TileInfo {
+  int p, b, m_tile, n_tile;
+};
+
+__device__ __forceinline__ TileInfo decode_tile(const GemmParams& P, int t) {
+  TileInfo ti;
+  ti.p = (P.nprob > 1 && t >= P.prob[1].tile_begin) ? 1 : 0;
+  const DevProblem& pr = P.prob[ti.p];
+  const int local = t - pr.tile_begin;
+  const int per_b = pr.m_tiles * pr.n_tiles;
+  ti.b = local / per_b;
+  const int r = local - ti.b * per_b;
+  ti.n_tile = r / pr.m_tiles;
+  ti.m_tile = r - ti.n_tile * pr.m_tiles;
+  return ti;
+}
+
+// Wait sites, reported through DeviceStatus::where.
+enum : uint32_t { kSiteEmpty = 0x101, kSiteFull = 0x102, kSiteAccEmpty = 0x103, kSiteAccFull = 0x104 };
+
+__device__ __forceinline__ void store_row32(bf16* dst, const float* f) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    d[i] = make_uint4(pack_bf16x2(f[8 * i + 0], f[8 * i + 1]), pack_bf16x2(f[8 * i + 2], f[8 * i + 3]),
+                      pack_bf16x2(f[8 * i + 4], f[8 * i + 5]), pack_bf16x2(f[8 * i + 6], f[8 * i + 7]));
+}
+
+__device__ __forceinline__ void load_row32(const bf16* src, float* f) {
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 u = s[i];
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 v = unpack_bf16x2(w[j]);
+      f[8 * i + 2 * j] = v.x;
+      f[8 * i + 2 * j + 1] = v.y;
+    }
+  }
+}
+
+__device__ __forceinline__ void store_row32_f32(float* dst, const float* f) {
+  float4* d = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) d[i] = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
+}
+
+__device__ __forceinline__ void load_row32_f32(const float* src, float* f) {
+  const float4* s4 = reinterpret_cast<const float4*>(src);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float4 v = s4[i];
+    f[4 * i] = v.x;
+    f[4 * i + 1] = v.y;
+    f[4 * i + 2] = v.z;
+    f[4 * i + 3] = v.w;
+  }
+}
+
+// SwiGLU over one packed 256-column accumulator: 128 outputs at dst[0..128).
+__device__ __forceinline__ void epi_swiglu(uint32_t tbase, bool row_ok, bf16* dst, int cols_left) {
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    uint32_t g[32], u[32];
+    tmem_load32(tbase + c * 32, g);
+    tmem_load32(tbase + 128 + c * 32, u);
+    if (row_ok && c * 32 < cols_left) {
+      float o[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) o[i] = silu_f(__uint_as_float(g[i])) * __uint_as_float(u[i]);
+      store_row32(dst + c * 32, o);
+    }
+  }
+}
+
+__device__ __forceinline__ void epi_qkv_head(uint32_t tb, bool row_ok, int which, bf16* dst, const bf16* nw,
+                                             const float* rope_row, float eps) {
+  if (which == 2) {
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      uint32_t v[32];
+      tmem_load32(tb + c * 32, v);
+      if (row_ok) {
+        float o[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(v[i]);
+        store_row32(dst + c * 32, o);
+      }
+    }
+    return;
+  }
+  float ss = 0.f;
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    uint32_t v[32];
+    tmem_load32(tb + c * 32, v);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float x = __uint_as_float(v[i]);
+      ss += x * x;
+    }
+  }
+  const float rs = rsqrtf(ss * (1.0f / 128.0f) + eps);
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    uint32_t v[32];
+    tmem_load32(tb + c * 32, v);
+    if (row_ok) {
+      float o[32];
+      const float4* rp = reinterpret_cast<const float4*>(rope_row + c * 32);  // 16 pairs (cos, sin)
+#pragma unroll
+      for (int p = 0; p < 16; p += 2) {
+        const float4 cs = __ldg(rp + p / 2);  // pair p: (cs.x, cs.y), pair p+1: (cs.z, cs.w)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int d = 2 * (p + h);
+          const float c0 = h ? cs.z : cs.x, s0 = h ? cs.w : cs.y;
+          const float x0 = __uint_as_float(v[d]) * rs * __bfloat162float(nw[c * 32 + d]);
+          const float x1 = __uint_as_float(v[d + 1]) * rs * __bfloat162float(nw[c * 32 + d + 1]);
+          o[d] = x0 * c0 - x1 * s0;
+          o[d + 1] = x0 * s0 + x1 * c0;
+        }
+      }
+      store_row32(dst + c * 32, o);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmParams P) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStages * kATileBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* acc_full = empty + kStages;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int p = 0; p < P.nprob; ++p) {
+      tma_prefetch_desc(&P.a_map[p]);
+      tma_prefetch_desc(&P.b_map[p]);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtx wc{P.status, abort_flag, kWaitLimitNs};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      long long issued = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < P.total_tiles && ok; t += gridDim.x) {
+        const TileInfo ti = decode_tile(P, t);
+        const DevProblem& pr = P.prob[ti.p];
+        const int kblocks = (pr.k + BK - 1) / BK;
+        const int arow = pr.a_row0 + ti.m_tile * BM;
+        const int brow = ti.n_tile * BN;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, wc, kSiteEmpty)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], kStageBytes);
+          tma_load_3d(sA + stage * kATileBytes, &P.a_map[ti.p], &full[stage], kb * BK, arow, ti.b);
+          tma_load_2d(sB + stage * kBTileBytes, &P.b_map[ti.p], &full[stage], kb * BK, brow);
+          ++issued;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // Unwinding: let the copies already issued land before the block exits.
+        const long long outstanding = issued < kStages ? issued : kStages;
+        for (long long i = 0; i < outstanding; ++i) {
+          if (stage == 0) {
+            stage = kStages;
+            phase ^= 1u;
+          }
+          --stage;
+          const uint64_t t0 = global_timer_ns();
+          while (!mbar_try(&full[stage], phase) && global_timer_ns() - t0 < 100000000ull) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = make_idesc_bf16(BM, BN, false);
+      uint32_t stage = 0, phase = 0;
+      int local = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < P.total_tiles && ok; t += gridDim.x, ++local) {
+        const TileInfo ti = decode_tile(P, t);
+        const DevProblem& pr = P.prob[ti.p];
+        const int kblocks = (pr.k + BK - 1) / BK;
+        const int acc = local & 1;
+        if (!mbar_wait(&acc_empty[acc], ((uint32_t)(local >> 1) & 1u) ^ 1u, wc, kSiteAccEmpty)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(&full[stage], phase, wc, kSiteFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(sA + stage * kATileBytes);
+          const uint32_t b_base = smem_u32(sB + stage * kBTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = make_sdesc_sw128(a_base + kk * 32, 16, 1024);
+            const uint64_t bd = make_sdesc_sw128(b_base + kk * 32, 16, 1024);
+            umma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit(&empty[stage]);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&acc_full[acc]);
+      }
+      // Every MMA this thread issued must be complete before TMEM is released.
+      umma_commit(drain);
+      const uint64_t t0 = global_timer_ns();
+      while (!mbar_try(drain, 0) && global_timer_ns() - t0 < 1000000000ull) {
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    int local = 0;
+    for (int t = blockIdx.x; t < P.total_tiles; t += gridDim.x, ++local) {
+      const int acc = local & 1;
+      bool ok = mbar_wait(&acc_full[acc], (uint32_t)(local >> 1) & 1u, wc, kSiteAccFull);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const TileInfo ti = decode_tile(P, t);
+      const DevProblem& pr = P.prob[ti.p];
+      const uint32_t tbase = tmem + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
+      const int r = ti.m_tile * BM + q * 32 + lane;
+      const bool row_ok = r < pr.rows;
+      const int col0 = ti.n_tile * BN;
+      if (pr.epi == kEpiStore || pr.epi == kEpiResidual) {
+        const long long off = (long long)ti.b * pr.out_bstride + (long long)(pr.out_row0 + r) * pr.ld_out +
+                              pr.out_col0 + col0;
+        const bf16* grow = pr.gate ? pr.gate + (long long)ti.b * pr.gate_stride + col0 : nullptr;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          tmem_load32(tbase + c * 32, v);
+          if (row_ok && col0 + c * 32 < pr.n) {
+            float o[32];
+            if (pr.epi == kEpiResidual) {
+              float xr[32];
+              if (pr.res_f32) load_row32_f32(pr.res_f32 + off + c * 32, xr);
+              else load_row32(pr.res + off + c * 32, xr);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = xr[i] + __bfloat162float(grow[c * 32 + i]) * __uint_as_float(v[i]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(v[i]);
+            }
+            if (pr.out_f32) store_row32_f32(pr.out_f32 + off + c * 32, o);
+            else store_row32(pr.out + off + c * 32, o);
+          }
+        }
+      } else if (pr.epi == kEpiSwiGLU || (pr.epi == kEpiQKV && col0 >= pr.n_qkv)) {
+        const int ocol = (col0 - (pr.epi == kEpiQKV ? pr.n_qkv : 0)) / 2;
+        const int n_out = (pr.n - (pr.epi == kEpiQKV ? pr.n_qkv : 0)) / 2;
+        bf16* orow = pr.out + (long long)ti.b * pr.out_bstride + (long long)(pr.out_row0 + r) * pr.ld_out +
+                     pr.out_col0 + ocol;
+        epi_swiglu(tbase, row_ok, orow, n_out - ocol);
+      } else {
+        const int which = col0 / pr.hidden;
+        const int heads = pr.hidden / 128;
+        const int tok = pr.tok0 + r;
+        bf16* base = which == 0 ? pr.q : (which == 1 ? pr.kk : pr.v);
+        const bf16* nw = which == 0 ? pr.q_norm : pr.k_norm;
+        const float* rope_row = pr.rope + (long long)(row_ok ? tok : 0) * 128;
+#pragma unroll 1
+        for (int hh = 0; hh < BN / 128; ++hh) {
+          const int head = (col0 % pr.hidden) / 128 + hh;
+          bf16* dst = base + (((long long)ti.b * heads + head) * pr.seq + tok) * 128;
+          epi_qkv_head(tbase + hh * 128, row_ok, which, dst, nw, rope_row, P.eps);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[acc]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+bool g_attr_set[16] = {false};
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmProblemHost* probs, int nprob, int batch, float eps, DeviceStatus* status,
+                        int cls, cudaStream_t s) {
+  if (nprob < 1 || nprob > 2) return cudaErrorInvalidValue;
+  GemmParams P;
+  memset(&P, 0, sizeof(P));
+  int tiles = 0;
+  for (int i = 0; i < nprob; ++i) {
+    const GemmProblemHost& h = probs[i];
+    DevProblem& d = P.prob[i];
+    if (h.rows <= 0 || h.n <= 0 || h.k <= 0) return cudaErrorInvalidValue;
+    const uint64_t adims[3] = {(uint64_t)h.k, (uint64_t)h.a_rows_total, (uint64_t)batch};
+    const uint64_t astr[2] = {(uint64_t)h.lda * 2, (uint64_t)h.lda * 2 * (uint64_t)h.a_rows_total};
+    const uint32_t abox[3] = {BK, BM, 1};
+    if (!encode_tmap_bf16(&P.a_map[i], h.a, 3, adims, astr, abox)) return cudaErrorInvalidValue;
+    const uint64_t bdims[2] = {(uint64_t)h.k, (uint64_t)h.n};
+    const uint64_t bstr[1] = {(uint64_t)h.k * 2};
+    const uint32_t bbox[2] = {BK, BN};
+    if (!encode_tmap_bf16(&P.b_map[i], h.w, 2, bdims, bstr, bbox)) return cudaErrorInvalidValue;
+    d.rows = h.rows;
+    d.a_row0 = h.a_row0;
+    d.n = h.n;
+    d.k = h.k;
+    d.m_tiles = (h.rows + BM - 1) / BM;
+    d.n_tiles = (h.n + BN - 1) / BN;
+    d.tile_begin = tiles;
+    d.epi = h.epi;
+    d.out = h.out;
+    d.out_f32 = h.out_f32;
+    d.res = h.res;
+    d.res_f32 = h.res_f32;
+    if (h.epi == kEpiResidual && !h.res && !h.res_f32) d.res = h.out;
+    d.out_bstride = h.out_bstride;
+    d.ld_out = h.ld_out;
+    d.out_row0 = h.out_row0;
+    d.out_col0 = h.out_col0;
+    d.gate = h.gate;
+    d.gate_stride = h.gate_stride;
+    d.n_qkv = h.n_qkv;
+    d.hidden = h.hidden;
+    d.q = h.q;
+    d.kk = h.kk;
+    d.v = h.v;
+    d.q_norm = h.q_norm;
+    d.k_norm = h.k_norm;
+    d.rope = h.rope;
+    d.seq = h.seq;
+    d.tok0 = h.tok0;
+    tiles += d.m_tiles * d.n_tiles * batch;
+  }
+  P.nprob = nprob;
+  P.batch = batch;
+  P.total_tiles = tiles;
+  P.eps = eps;
+  P.status = status;
+  if (tiles == 0) return cudaSuccess;
+
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 16 && !g_attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    g_attr_set[dev] = true;
+  }
+  const int sms = sm_count();
+  const int grid = tiles < sms ? tiles : sms;
+  LaunchScope scope(cls, s);
+  gemm_kernel<<<grid, kThreads, kSmemBytes, s>>>(P);
+  return cudaGetLastError();
+}
+
+}  // namespace dit

@@ -1,0 +1,261 @@
+/*
+ * dit.h -- C ABI of the GB300 (sm_103a) library for one FLUX.2 [klein]-style DiT
+ * denoising step.
+ *
+ * What the step computes (sources, by page title and section):
+ *   - "flux2-klein-p100a" model card, task table: 4 steps, guidance 1.0, no CFG, so each
+ *     step is one DiT call; Caveats: all 512 padded text rows enter the DiT with no mask,
+ *     text features are encoder layers 9, 18, 27 concatenated to [512, 7680], and the
+ *     modulation is global per step, not per block.
+ *   - "tt_flux2_klein -- Python reference", Modules: tt_dit.py runs 5 dual-stream and
+ *     20 single-stream blocks; host.py builds the token ids and RoPE; "Things that are
+ *     easy to get wrong": RoPE is 32 dims per axis at theta 2000 on adjacent pairs, and
+ *     reference image i gets t = 10 + 10*i.
+ *   The pages do not write the block maths out; the readings this library implements
+ *   (LayerNorm eps 1e-6, (1 + scale) LN(x) + shift, raw gates, per-head QK-RMSNorm
+ *   before RoPE, SwiGLU with the gate first, no biases, sinusoidal timestep embedding of
+ *   1000*sigma) are stated beside each entry point.
+ *
+ * Conventions for every entry point:
+ *   - Pointers marked "dev" are caller-owned device memory, 16-byte aligned; "host" ones
+ *     are host memory.  The library never allocates device memory in these calls and
+ *     never frees caller memory.  Weights stay owned by the caller; the structs below
+ *     hold pointers only.
+ *   - Tensors are bf16 (raw 16-bit storage) unless stated; row-major; "[A, B]" lists the
+ *     outermost dimension first.
+ *   - Device work is enqueued asynchronously on `stream` (NULL = the legacy default
+ *     stream).  A return value reports what was known at launch time only.
+ *   - Every argument is validated before anything is launched.  An invalid argument
+ *     returns DIT_ERR_INVALID_ARG, an unsupported configuration DIT_ERR_UNSUPPORTED, a
+ *     too-small workspace DIT_ERR_WORKSPACE; in those cases nothing is launched and no
+ *     memory is touched.  A failed launch returns DIT_ERR_CUDA.
+ *   - Kernels never trap or spin forever: a device-side wait that runs past its limit
+ *     writes a status word in the workspace and the kernel unwinds; dit_sync_status()
+ *     reports it as DIT_ERR_TIMEOUT.
+ *   - No C++ exception crosses this boundary.  Calls on different workspaces and
+ *     streams may run concurrently from different host threads, except the timing
+ *     functions (dit_timing_*), which use process-wide state.
+ */
+#ifndef DIT_H_
+#define DIT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same handle as cudaStream_t. */
+typedef struct CUstream_st* dit_stream_t;
+
+typedef enum {
+  DIT_OK = 0,
+  DIT_ERR_INVALID_ARG = 1,
+  DIT_ERR_UNSUPPORTED = 2,
+  DIT_ERR_WORKSPACE = 3,
+  DIT_ERR_CUDA = 4,
+  DIT_ERR_TIMEOUT = 5
+} dit_status;
+
+/* Model widths.  Supported: head_dim == 128, hidden == heads * 128, hidden % 256 == 0,
+ * hidden <= 8192, mlp_hidden % 128 == 0, in_channels % 32 == 0, txt_dim % 8 == 0,
+ * axes_dim[i] even with sum == head_dim, rope_theta > 0, eps > 0.
+ * klein 4B: {3072, 24, 128, 9216, 5, 20, 128, 7680, 2000.f, {32,32,32,32}, 1e-6f}. */
+typedef struct {
+  int hidden, heads, head_dim, mlp_hidden, n_dual, n_single, in_channels, txt_dim;
+  float rope_theta;
+  int axes_dim[4];
+  float eps;
+} dit_config;
+
+/* Joint sequence of one step: per batch row, rows [text | target image | references];
+ * N = n_txt + n_img + n_ref.  n_txt >= 1, n_img >= 1, n_ref >= 0, 1 <= batch <= 64. */
+typedef struct {
+  int batch, n_txt, n_img, n_ref;
+} dit_shape;
+
+/* Timestep MLP and the global modulation projection: t_in [H, 256], t_out [H, H],
+ * mod [17H, H]. */
+typedef struct {
+  const void *t_in, *t_out, *mod;
+} dit_mod_weights;
+
+/* One stream of a dual-stream block: qkv [3H, H] (rows q | k | v), q_norm [128],
+ * k_norm [128], out [H, H], mlp_in [2F, H] in the PACKED layout of dit_pack_mlp_in,
+ * mlp_out [H, F].  No biases. */
+typedef struct {
+  const void *qkv, *q_norm, *k_norm, *out, *mlp_in, *mlp_out;
+} dit_stream_weights;
+
+typedef struct {
+  dit_stream_weights img, txt;
+} dit_dual_weights;
+
+/* A single-stream block: qkv_mlp [3H + 2F, H] whose first 3H rows are q | k | v and
+ * whose last 2F rows are the MLP-in in the PACKED layout of dit_pack_mlp_in;
+ * q_norm [128], k_norm [128]; out [H, H + F] over the concatenation [attn | act]. */
+typedef struct {
+  const void *qkv_mlp, *q_norm, *k_norm, *out;
+} dit_single_weights;
+
+/* All weights.  `dual` and `single` are HOST arrays of n_dual and n_single entries
+ * (they hold device pointers); they must stay valid for the duration of each call.
+ * x_emb [H, in_channels], ctx_emb [H, txt_dim], proj_out [in_channels, H]. */
+typedef struct {
+  dit_config cfg;
+  dit_mod_weights mod;
+  const void *x_emb, *ctx_emb, *proj_out;
+  const dit_dual_weights* dual;
+  const dit_single_weights* single;
+} dit_weights;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* dit_status_string(dit_status s);
+
+/* Fill *cfg with the klein 4B widths listed above. */
+dit_status dit_config_klein(dit_config* cfg);
+
+/* Bytes of workspace that every *_fwd / dit_modulation / dit_attention call on this
+ * config and shape needs (the largest of them; dit_step_host included).  The workspace
+ * is caller-owned device memory; its first 256 bytes hold the device status word and
+ * must be zeroed once by the caller before first use (the library clears it again in
+ * dit_sync_status). */
+dit_status dit_workspace_size(const dit_config* cfg, const dit_shape* shape, size_t* bytes);
+
+/* Host maths: the (t, h, w, l) position id of every row of the joint sequence, written
+ * to ids_host [N, 4] int32.  Text row i: (0, 0, 0, i), padded rows continuing the
+ * count; target token (r, c) of the grid_h x grid_w patch grid, row-major: (0, r, c, 0);
+ * reference i (ref_grids_host[2i] rows x ref_grids_host[2i+1] cols, row-major):
+ * (10 + 10*i, r, c, 0) ("tt_flux2_klein -- Python reference", "Things that are easy to
+ * get wrong", and Modules: host.py).  Requires grid_h * grid_w == shape->n_img and the
+ * reference grids to sum to shape->n_ref.  Runs on the host; touches no device. */
+dit_status dit_token_ids(const dit_shape* shape, int grid_h, int grid_w, const int* ref_grids_host, int n_refs,
+                         int32_t* ids_host);
+
+/* RoPE table of a sequence: for every row and every adjacent pair p of the 128-dim head
+ * (axis a owns dims [sum(axes_dim[<a]), +axes_dim[a]); its pair j turns by
+ * pos_a * theta^(-2j / axes_dim[a])), table_dev[(row * 64 + p) * 2 + {0, 1}] =
+ * {cos, sin} as fp32, angles evaluated in fp64 ("tt_flux2_klein -- Python reference",
+ * "Things that are easy to get wrong").  ids_dev [n, 4] int32 device, table_dev
+ * [n, 64, 2] fp32 device.  Build it once per shape; every block call reads it. */
+dit_status dit_rope_table(const dit_config* cfg, const int32_t* ids_dev, int n, float* table_dev,
+                          dit_stream_t stream);
+
+/* Weight preparation: rearrange an MLP-in weight from the logical order [gate (F rows);
+ * up (F rows)] into the packed order the library reads: blocks of 256 rows, block j =
+ * [gate rows 128j .. 128j+127 ; up rows 128j .. 128j+127].  src_dev and dst_dev are
+ * [2F, cols] bf16 device buffers that must not overlap.  For a single-stream qkv_mlp
+ * weight, pack its last 2F rows (pointer offset 3H * cols elements) and copy the first
+ * 3H rows unchanged. */
+dit_status dit_pack_mlp_in(const void* src_dev, void* dst_dev, int mlp_hidden, int cols, dit_stream_t stream);
+
+/* Global modulation of one step ("flux2-klein-p100a" Caveats: computed once per step and
+ * shared by all blocks).  tau = 1000 * sigma; s = [cos(tau f_k) | sin(tau f_k)],
+ * f_k = 10000^(-k/128), k < 128; e = t_out SiLU(t_in s); m = mod SiLU(e).
+ * sigma_dev [batch] fp32 device; mod_dev [batch, 17H] bf16 device, slots in order
+ * img-dual (shift_a, scale_a, gate_a, shift_m, scale_m, gate_m), txt-dual (same six),
+ * single (shift, scale, gate), final (shift, scale).  Uses the workspace as scratch. */
+dit_status dit_modulation(const dit_weights* w, const float* sigma_dev, int batch, void* mod_dev, void* ws,
+                          size_t ws_bytes, dit_stream_t stream);
+
+/* One dual-stream block `layer` (0 <= layer < n_dual), in place on x_dev [B, N, H]
+ * (rows text | image | reference).  Per stream s (text rows use `txt`, image and
+ * reference rows use `img` weights and modulation):
+ *   y = (1 + scale_a) LN(x) + shift_a;  q, k, v = y qkv^T;  q, k <- RMSNorm_head * w;
+ *   q, k <- RoPE;  o = joint softmax attention over all N rows, no mask;
+ *   x += gate_a (o out^T);  y = (1 + scale_m) LN(x) + shift_m;
+ *   x += gate_m (silu(y gate^T) * (y up^T)) mlp_out^T.
+ * mod_dev [B, 17H] from dit_modulation; rope_dev [N, 64, 2] from dit_rope_table. */
+dit_status dit_dual_block_fwd(const dit_weights* w, int layer, const dit_shape* shape, void* x_dev,
+                              const void* mod_dev, const float* rope_dev, void* ws, size_t ws_bytes,
+                              dit_stream_t stream);
+
+/* One single-stream block `layer` (0 <= layer < n_single), in place on x_dev [B, N, H]:
+ *   y = (1 + scale) LN(x) + shift;  [q | k | v | gate | up] = y qkv_mlp^T;
+ *   q, k <- RMSNorm_head * w, RoPE;  o = attention;  act = silu(gate) * up;
+ *   x += gate_s ([o | act] out^T).  Other arguments as dit_dual_block_fwd. */
+dit_status dit_single_block_fwd(const dit_weights* w, int layer, const dit_shape* shape, void* x_dev,
+                                const void* mod_dev, const float* rope_dev, void* ws, size_t ws_bytes,
+                                dit_stream_t stream);
+
+/* One whole DiT step (one velocity evaluation): modulation from sigma, embedders
+ * (img/ref tokens by x_emb, text by ctx_emb) into the joint stream, n_dual dual blocks,
+ * n_single single blocks, then the final layer (1 + scale_f) LN(x) + shift_f and
+ * proj_out on the target-image rows only.
+ * img_tokens [B, n_img, C], ref_tokens [B, n_ref, C] (NULL iff n_ref == 0),
+ * txt_emb [B, n_txt, txt_dim], rope_dev [N, 64, 2] fp32, sigma_dev [B] fp32,
+ * velocity_out [B, n_img, C]; all device. */
+dit_status dit_step_fwd(const dit_weights* w, const dit_shape* shape, const void* img_tokens,
+                        const void* ref_tokens, const void* txt_emb, const float* rope_dev, const float* sigma_dev,
+                        void* velocity_out, void* ws, size_t ws_bytes, dit_stream_t stream);
+
+/* dit_step_fwd with HOST inputs and output: copies img_tokens, ref_tokens, txt_emb and
+ * sigma (host, same layouts; pinned memory gives asynchronous copies) into the
+ * workspace, runs the step and copies the velocity back to velocity_host, all on
+ * `stream`.  The result is valid once the stream has completed. */
+dit_status dit_step_host(const dit_weights* w, const dit_shape* shape, const void* img_tokens_host,
+                         const void* ref_tokens_host, const void* txt_emb_host, const float* rope_dev,
+                         const float* sigma_host, void* velocity_host, void* ws, size_t ws_bytes,
+                         dit_stream_t stream);
+
+/* Synchronise `stream`, read and clear the workspace's device status word.  Returns
+ * DIT_ERR_TIMEOUT if a kernel gave up on a wait since the last call, else DIT_OK
+ * (or DIT_ERR_CUDA if the stream reports an error).  *where_out (may be NULL) receives
+ * the id of the first wait that gave up. */
+dit_status dit_sync_status(void* ws, dit_stream_t stream, uint32_t* where_out);
+
+/* ---- Component operations (the kernels a block is made of) ---------------------- */
+
+/* Adaptive LayerNorm on rows of x: for batch b and row r < rows,
+ * y[b, r] = (1 + scale_b) LN(x[b, x_row0 + r]) + shift_b, LN without affine, biased
+ * variance, eps from the argument, statistics in fp32.  Rows r < split use
+ * (shift_lo, scale_lo), the others (shift_hi, scale_hi); each vector [hidden] lives at
+ * pointer + b * mod_stride elements.  x_dev [B, x_rows, hidden], y_dev [B, rows, hidden]. */
+dit_status dit_adaln(int batch, int rows, int hidden, const void* x_dev, int x_rows, int x_row0, int split,
+                     const void* shift_lo, const void* scale_lo, const void* shift_hi, const void* scale_hi,
+                     long long mod_stride, float eps, void* y_dev, dit_stream_t stream);
+
+typedef enum {
+  DIT_EPI_STORE = 0,          /* out = A W^T                                        */
+  DIT_EPI_GATED_RESIDUAL = 1, /* out += gate_b * (A W^T), gate at gate + b*gate_stride */
+  DIT_EPI_SWIGLU = 2          /* out = silu(A Wg^T) * (A Wu^T), W packed (2*n_out rows) */
+} dit_epilogue;
+
+/* Linear layer on the tensor cores: a_dev [B, rows, k], w_dev [n_w, k] (n_w = n_out,
+ * or 2*n_out packed for SWIGLU), out_dev [B, rows, ld_out] written at columns
+ * [0, n_out).  k % 8 == 0, n_out % 32 == 0 (SWIGLU: n_out % 128 == 0), ld_out % 8 == 0.
+ * ws: any workspace of >= 256 bytes (only its status word is used). */
+dit_status dit_linear(int batch, int rows, int n_out, int k, const void* a_dev, const void* w_dev, void* out_dev,
+                      int ld_out, dit_epilogue epi, const void* gate_dev, long long gate_stride, void* ws,
+                      size_t ws_bytes, dit_stream_t stream);
+
+/* Joint attention: q/k/v_dev [B, heads, n, 128] bf16 (head-major), softmax over all n
+ * keys with scale 1/sqrt(128), no mask; out_dev [B, n, ld_out] with head h written at
+ * columns [128h, 128h + 128).  ld_out % 8 == 0, ld_out >= 128 * heads.  ws: any
+ * workspace of >= 256 bytes (only its status word is used). */
+dit_status dit_attention(int batch, int heads, int n, const void* q_dev, const void* k_dev, const void* v_dev,
+                         void* out_dev, int ld_out, void* ws, size_t ws_bytes, dit_stream_t stream);
+
+/* ---- Measurement ------------------------------------------------------------------ */
+
+/* Kernel launches issued by this library since it was loaded (all entry points). */
+unsigned long long dit_launch_count(void);
+
+/* Start recording a CUDA event pair around every kernel launch (up to max_records
+ * launches), tagged with the kernel's class (dit_kernel_class_name).  Events are
+ * recorded on the launch's own stream. */
+dit_status dit_timing_begin(int max_records);
+
+/* Stop recording, synchronise the recorded events and return up to `cap` records:
+ * classes[i] and ms[i] (device time of launch i).  *n receives the count. */
+dit_status dit_timing_end(int* n, int* classes, float* ms, int cap);
+
+/* Static name of a kernel class id, or "?" for an unknown id. */
+const char* dit_kernel_class_name(int cls);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DIT_H_ */

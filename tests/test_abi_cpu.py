@@ -1,0 +1,130 @@
+"""The C ABI without a GPU: the library loads, exports every symbol include/dit.h declares,
+validates arguments before touching any device, and its host maths (token ids) equals
+the oracle's bit for bit."""
+import ctypes as C
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle import dit_oracle as O
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dit.h")
+
+
+@pytest.fixture(scope="module")
+def dit():
+    from diffusion_transformer_step_gb300 import build_lib
+    build_lib.build()
+    from diffusion_transformer_step_gb300 import dit as d
+    d.lib()
+    return d
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_ ]*\*?\s+\**(dit_[a-z0-9_]+)\s*\(", src, re.M)))
+
+
+def test_every_declared_symbol_is_exported(dit):
+    names = declared_functions()
+    assert len(names) >= 19, names
+    L = dit.lib()
+    for n in names:
+        assert hasattr(L, n), n
+    # and the binding wraps every one of them under the same name
+    for n in names:
+        assert n in dit._SIGS, n
+
+
+def test_status_strings_and_klein_config(dit):
+    for s in range(6):
+        assert dit.dit_status_string(s)
+    c = dit.dit_config_klein()
+    assert (c.hidden, c.heads, c.head_dim, c.mlp_hidden, c.n_dual, c.n_single, c.in_channels, c.txt_dim) == \
+        (3072, 24, 128, 9216, 5, 20, 128, 7680)
+    assert abs(c.rope_theta - 2000.0) < 1e-3 and list(c.axes_dim) == [32, 32, 32, 32]
+
+
+def test_token_ids_equal_oracle(dit):
+    for n_txt, gh, gw, refs in ((512, 64, 64, ()), (512, 68, 120, ((64, 64),)), (3, 2, 3, ((1, 2), (2, 1))),
+                                (7, 5, 3, ((2, 2), (3, 1), (1, 4)))):
+        nref = sum(a * b for a, b in refs)
+        shape = dit.make_shape(1, n_txt, gh * gw, nref)
+        got = dit.dit_token_ids(shape, gh, gw, refs).numpy()
+        np.testing.assert_array_equal(got, O.token_ids(n_txt, gh, gw, refs))
+
+
+def test_token_ids_rejects_inconsistent_grid(dit):
+    shape = dit.make_shape(1, 4, 10, 0)
+    with pytest.raises(dit.DitError) as e:
+        dit.dit_token_ids(shape, 3, 3)
+    assert e.value.status == dit.DIT_ERR_INVALID_ARG
+
+
+def test_workspace_size_grows_with_shape(dit):
+    c = dit.dit_config_klein()
+    a = dit.dit_workspace_size(c, dit.make_shape(1, 512, 4096, 0))
+    b = dit.dit_workspace_size(c, dit.make_shape(4, 512, 8160, 4096))
+    assert 0 < a < b
+    # 5 activation buffers of [N, H] + concat [N, H+F] dominate
+    N, H, F = 4608, 3072, 9216
+    assert a > N * H * 2 * 5 + N * (H + F) * 2
+
+
+def test_unsupported_configs_rejected(dit):
+    shape = dit.make_shape(1, 8, 16, 0)
+    for field, val in (("head_dim", 64), ("hidden", 3000), ("mlp_hidden", 100), ("in_channels", 20),
+                       ("txt_dim", 7)):
+        c = dit.dit_config_klein()
+        setattr(c, field, val)
+        n = C.c_size_t(0)
+        st = dit.lib().dit_workspace_size(C.byref(c), C.byref(shape), C.byref(n))
+        assert st == dit.DIT_ERR_UNSUPPORTED, (field, st)
+    c = dit.dit_config_klein()
+    c.axes_dim[0] = 30
+    assert dit.lib().dit_workspace_size(C.byref(c), C.byref(shape), C.byref(C.c_size_t())) == dit.DIT_ERR_UNSUPPORTED
+
+
+def test_invalid_arguments_rejected_before_any_launch(dit):
+    """Each call fails validation without a device; the launch counter must not move."""
+    L = dit.lib()
+    before = dit.dit_launch_count()
+    c = dit.dit_config_klein()
+    shape = dit.make_shape(1, 512, 4096, 0)
+    w = dit.dit_weights()
+    w.cfg = c
+    fake = 0x10000  # aligned, never dereferenced: validation fails on another argument first
+    # null weights / misaligned pointers / bad layer / bad batch / small workspace
+    assert L.dit_dual_block_fwd(None, 0, C.byref(shape), fake, fake, fake, fake, 1 << 40, None) == dit.DIT_ERR_INVALID_ARG
+    assert L.dit_dual_block_fwd(C.byref(w), 0, C.byref(shape), fake + 2, fake, fake, fake, 1 << 40, None) == dit.DIT_ERR_INVALID_ARG
+    assert L.dit_dual_block_fwd(C.byref(w), 7, C.byref(shape), fake, fake, fake, fake, 1 << 40, None) == dit.DIT_ERR_INVALID_ARG
+    assert L.dit_single_block_fwd(C.byref(w), 0, C.byref(shape), fake, fake, fake, fake, 1024, None) == dit.DIT_ERR_WORKSPACE
+    bad = dit.make_shape(0, 512, 4096, 0)
+    assert L.dit_single_block_fwd(C.byref(w), 0, C.byref(bad), fake, fake, fake, fake, 1 << 40, None) == dit.DIT_ERR_INVALID_ARG
+    assert L.dit_step_fwd(C.byref(w), C.byref(shape), fake, None, fake, fake, fake, fake, fake, 1 << 40, None) == dit.DIT_ERR_INVALID_ARG
+    assert L.dit_modulation(C.byref(w), fake, 0, fake, fake, 1 << 20, None) == dit.DIT_ERR_INVALID_ARG
+    assert L.dit_rope_table(C.byref(c), fake + 4, 10, fake, None) == dit.DIT_ERR_INVALID_ARG
+    assert L.dit_pack_mlp_in(fake, fake + 16, 9216, 3072, None) == dit.DIT_ERR_INVALID_ARG   # overlap
+    assert L.dit_pack_mlp_in(fake, fake, 100, 3072, None) == dit.DIT_ERR_INVALID_ARG
+    assert L.dit_linear(1, 10, 48, 64, fake, fake, fake, 48, 0, None, 0, fake, 256, None) == dit.DIT_ERR_INVALID_ARG  # n % 32
+    assert L.dit_linear(1, 10, 64, 60, fake, fake, fake, 64, 0, None, 0, fake, 256, None) == dit.DIT_ERR_INVALID_ARG  # k % 8
+    assert L.dit_linear(1, 10, 64, 64, fake, fake, fake, 64, 1, None, 0, fake, 256, None) == dit.DIT_ERR_INVALID_ARG  # no gate
+    assert L.dit_linear(1, 10, 64, 64, fake, fake, fake, 64, 0, None, 0, fake, 16, None) == dit.DIT_ERR_WORKSPACE
+    assert L.dit_attention(1, 2, 10, fake, fake, fake, fake, 200, fake, 256, None) == dit.DIT_ERR_INVALID_ARG  # ld < 256
+    assert L.dit_adaln(1, 4, 300, fake, 4, 0, 0, fake, fake, fake, fake, 0, 1e-6, fake, None) == dit.DIT_ERR_UNSUPPORTED
+    assert L.dit_adaln(1, 4, 256, fake, 3, 0, 0, fake, fake, fake, fake, 0, 1e-6, fake, None) == dit.DIT_ERR_INVALID_ARG
+    assert L.dit_timing_begin(0) == dit.DIT_ERR_INVALID_ARG
+    assert dit.dit_launch_count() == before
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch, dit):
+    import importlib
+    mod = importlib.reload(dit)
+    monkeypatch.setattr(mod, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(mod, "_lib", None)
+    with pytest.raises(RuntimeError):
+        mod.lib()

@@ -1,0 +1,182 @@
+"""GPU parity of whole blocks and of the whole step against the oracle, through the C ABI.
+
+Acceptance: per block output max-abs <= 3e-2 and cosine >= 0.999 (bf16 GPU path against
+the unrounded oracle on the same bf16 inputs); the full 25-block step cosine >= 0.995.
+Batch rows are independent ("FLUX.2 [klein] 4B/9B + Z-Image-Turbo on a shared DiT
+scaffold": rows independent of their batch neighbours bit for bit), so at batch 4 the
+oracle checks rows 0 and 3 and the GPU's own batch invariance covers the rest.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import dit_oracle as O
+from diffusion_transformer_step_gb300 import synth
+import helpers as Hx
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+BLOCK_ATOL, BLOCK_COS, STEP_COS = 3e-2, 0.999, 0.995
+
+TINY_REF = synth.Workload("tiny_ref_b2", synth.TINY, 2, 40, (7, 20), ((6, 10),))       # N = 240, ragged
+TINY_MULTI = synth.Workload("tiny_3ref", synth.TINY, 1, 24, (4, 6), ((2, 3), (3, 3), (1, 5)))
+
+
+@pytest.fixture(scope="module")
+def dit():
+    from diffusion_transformer_step_gb300 import build_lib
+    build_lib.build()
+    from diffusion_transformer_step_gb300 import dit as d
+    d.lib()
+    return d
+
+
+def _setup(dit, wl, W):
+    shape = dit.make_shape(wl.batch, wl.n_txt, wl.n_img, wl.n_ref)
+    ids = dit.dit_token_ids(shape, *wl.grid, wl.ref_grids)
+    N = wl.n_tokens
+    rope = torch.empty((N, 64, 2), dtype=torch.float32, device=DEV)
+    dit.dit_rope_table(W.cfg, ids.to(DEV), N, rope)
+    nbytes = dit.dit_workspace_size(W.cfg, shape)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device=DEV)
+    return shape, rope, ws, nbytes
+
+
+def _status(dit, ws):
+    st, where = dit.dit_sync_status(ws)
+    assert st == dit.DIT_OK, f"device wait gave up at site {where:#x}"
+
+
+def run_block(dit, kind, wl, seed=0, check_rows=None):
+    wd = wl.widths
+    g = synth.generator(seed)
+    if kind == "dual":
+        logical = {"dual": [(synth.stream_weights(wd, g), synth.stream_weights(wd, g))], "single": []}
+    else:
+        logical = {"dual": [], "single": [synth.single_weights(wd, g)]}
+    W = dit.DeviceWeights(wd, logical)
+    bi = synth.block_inputs(wl, seed)
+    shape, rope, ws, nbytes = _setup(dit, wl, W)
+    x = bi["x"].to(DEV).contiguous()
+    mod = bi["mod"].to(DEV).contiguous()
+    fwd = dit.dit_dual_block_fwd if kind == "dual" else dit.dit_single_block_fwd
+    fwd(W.w, 0, shape, x, mod, rope, ws, nbytes)
+    _status(dit, ws)
+    got = Hx.to_np(x)
+
+    big = wd.hidden > 1024
+    dt = np.float32 if big else np.float64
+    cfg = Hx.oracle_config(wd)
+    c, s = O.rope_table(O.token_ids(wl.n_txt, *wl.grid, wl.ref_grids))
+    c, s = c.astype(dt), s.astype(dt)
+    xin, m = Hx.to_np(bi["x"], dt), Hx.to_np(bi["mod"], dt)
+    rows = range(wl.batch) if check_rows is None else check_rows
+    for b in rows:
+        mod_b = O.split_modulation(m[b:b + 1], wd.hidden)
+        if kind == "dual":
+            img, txt = logical["dual"][0]
+            want = O.dual_block(xin[b:b + 1], wl.n_txt, Hx.oracle_stream(img, dt), Hx.oracle_stream(txt, dt), mod_b,
+                                c, s, cfg, dt)
+        else:
+            want = O.single_block(xin[b:b + 1], Hx.oracle_single(logical["single"][0], dt), mod_b, c, s, cfg, dt)
+        err, cs = Hx.max_abs(got[b:b + 1], want), Hx.cosine(got[b:b + 1], want)
+        # the block's change to x is what it computed: check its direction too
+        dcs = Hx.cosine(got[b:b + 1] - xin[b:b + 1], want - xin[b:b + 1])
+        print(f"{kind} {wl.name} row {b}: max_abs {err:.4g} cos {cs:.7f} delta-cos {dcs:.6f}")
+        assert err <= BLOCK_ATOL and cs >= BLOCK_COS and dcs >= 0.99, (b, err, cs, dcs)
+
+
+@pytest.mark.parametrize("kind", ["dual", "single"])
+@pytest.mark.parametrize("wl", [synth.WORKLOADS["tiny"], TINY_REF, TINY_MULTI], ids=lambda w: w.name)
+def test_block_tiny(dit, kind, wl):
+    run_block(dit, kind, wl, seed=1)
+
+
+def test_dual_block_klein_1024(dit):
+    run_block(dit, "dual", synth.WORKLOADS["dual_block_1024"], seed=0)
+
+
+def test_single_block_klein_1024(dit):
+    run_block(dit, "single", synth.WORKLOADS["single_block_1024"], seed=0)
+
+
+@pytest.mark.parametrize("kind", ["dual", "single"])
+def test_blocks_ref_1920x1088_b4(dit, kind):
+    run_block(dit, kind, synth.WORKLOADS["ref_1920x1088_b4"], seed=2, check_rows=[0, 3])
+
+
+def _step(dit, wl, logical, inp, W=None):
+    W = W or dit.DeviceWeights(wl.widths, logical)
+    shape, rope, ws, nbytes = _setup(dit, wl, W)
+    vel = torch.empty((wl.batch, wl.n_img, wl.widths.in_channels), dtype=torch.bfloat16, device=DEV)
+    ref = inp["ref_tokens"].to(DEV) if inp["ref_tokens"] is not None else None
+    dit.dit_step_fwd(W.w, shape, inp["img_tokens"].to(DEV), ref, inp["txt_emb"].to(DEV), rope,
+                     inp["sigma"].to(DEV), vel, ws, nbytes)
+    _status(dit, ws)
+    return vel, W
+
+
+def _oracle_step(wl, logical, inp, dt, rows):
+    ow = Hx.oracle_weights(wl.widths, logical, dt)
+    ids = O.token_ids(wl.n_txt, *wl.grid, wl.ref_grids)
+    out = []
+    for b in rows:
+        ref = Hx.to_np(inp["ref_tokens"][b:b + 1], dt) if inp["ref_tokens"] is not None else None
+        out.append(O.dit_step(ow, Hx.to_np(inp["img_tokens"][b:b + 1], dt), ref,
+                              Hx.to_np(inp["txt_emb"][b:b + 1], dt), Hx.to_np(inp["sigma"][b:b + 1]), ids, dt))
+    return np.concatenate(out, 0)
+
+
+@pytest.mark.parametrize("wl", [synth.WORKLOADS["tiny"], TINY_REF, TINY_MULTI], ids=lambda w: w.name)
+def test_step_tiny(dit, wl):
+    logical = synth.model_weights(wl.widths, seed=3)
+    inp = synth.step_inputs(wl, seed=3)
+    vel, _ = _step(dit, wl, logical, inp)
+    want = _oracle_step(wl, logical, inp, np.float64, range(wl.batch))
+    got = Hx.to_np(vel)
+    cs = Hx.cosine(got, want)
+    print(f"step {wl.name}: cos {cs:.6f} max_abs {Hx.max_abs(got, want):.4g}")
+    assert cs >= STEP_COS
+
+
+def test_step_host_buffers_match_device_buffers(dit):
+    wl = TINY_REF
+    logical = synth.model_weights(wl.widths, seed=4)
+    inp = synth.step_inputs(wl, seed=4)
+    vel, W = _step(dit, wl, logical, inp)
+    shape, rope, ws, nbytes = _setup(dit, wl, W)
+    pin = lambda t: t.contiguous().pin_memory()
+    out = torch.empty((wl.batch, wl.n_img, wl.widths.in_channels), dtype=torch.bfloat16).pin_memory()
+    dit.dit_step_host(W.w, shape, pin(inp["img_tokens"]), pin(inp["ref_tokens"]), pin(inp["txt_emb"]), rope,
+                      pin(inp["sigma"]), out, ws, nbytes)
+    _status(dit, ws)
+    assert torch.equal(out, vel.cpu())
+
+
+def test_step_klein_1024(dit):
+    """The full 25-block step at 1024x1024 against the fp32 oracle (about a minute of CPU)."""
+    wl = synth.WORKLOADS["step_1024"]
+    logical = synth.model_weights(wl.widths, seed=0)
+    inp = synth.step_inputs(wl, seed=0)
+    vel, W = _step(dit, wl, logical, inp)
+    del W
+    want = _oracle_step(wl, logical, inp, np.float32, [0])
+    got = Hx.to_np(vel)
+    cs = Hx.cosine(got, want)
+    print(f"step_1024: cos {cs:.6f} max_abs {Hx.max_abs(got, want):.4g}")
+    assert cs >= STEP_COS
+
+
+def test_step_batch_invariance_ref_b4(dit):
+    """Row b of the batch-4 reference-guided step equals the batch-1 step of row b, bit for bit."""
+    wl = synth.WORKLOADS["ref_1920x1088_b4"]
+    logical = synth.model_weights(wl.widths, seed=5, device=DEV)
+    inp = synth.step_inputs(wl, seed=5, device=DEV)
+    inp["sigma"] = torch.tensor([0.9, 0.7, 0.55, 0.95], dtype=torch.float32, device=DEV)
+    vel, W = _step(dit, wl, logical, inp)
+    assert torch.isfinite(vel.float()).all()
+    for b in (0, 3):
+        wl1 = synth.Workload("row", wl.widths, 1, wl.n_txt, wl.grid, wl.ref_grids)
+        one = {k: (v[b:b + 1] if v is not None else None) for k, v in inp.items()}
+        v1, _ = _step(dit, wl1, logical, one, W)
+        assert torch.equal(v1[0], vel[b]), b

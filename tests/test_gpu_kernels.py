@@ -1,0 +1,163 @@
+"""GPU parity of each kernel against the oracle, through the C ABI, on seeded inputs at
+sizes the oracle finishes in seconds that span several tiles and a ragged tail.
+
+Tolerances: every output is stored as bf16 (relative rounding 2^-9), inputs are the same
+bf16 values on both sides and all accumulation is fp32 on the GPU, so the bound is a
+few bf16 ulps of the output's magnitude: max-abs <= 3e-2 and cosine >= 0.9999 (0.999 for
+attention, whose P is rounded to bf16 before the PV product).
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import dit_oracle as O
+from diffusion_transformer_step_gb300 import synth
+import helpers as Hx
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def dit():
+    from diffusion_transformer_step_gb300 import build_lib
+    build_lib.build()
+    from diffusion_transformer_step_gb300 import dit as d
+    d.lib()
+    return d
+
+
+@pytest.fixture()
+def ws():
+    t = torch.zeros(1 << 20, dtype=torch.uint8, device=DEV)
+    return t
+
+
+def _check_status(dit, ws):
+    st, where = dit.dit_sync_status(ws)
+    assert st == dit.DIT_OK, f"device wait gave up at site {where:#x}"
+
+
+def _randn(shape, std=1.0, seed=0, mean=0.0):
+    g = synth.generator(seed)
+    return synth.normal(shape, std, g, mean=mean)
+
+
+def _cmp(got, want, atol=3e-2, cos_min=0.9999):
+    got = Hx.to_np(got)
+    err = Hx.max_abs(got, want)
+    cs = Hx.cosine(got, want)
+    assert np.isfinite(got).all()
+    assert err <= atol and cs >= cos_min, (err, cs)
+    return err, cs
+
+
+@pytest.mark.parametrize("n_txt,grid,refs", [(32, (8, 8), ()), (512, (64, 64), ()), (512, (68, 120), ((64, 64),))])
+def test_rope_table(dit, n_txt, grid, refs):
+    nref = sum(a * b for a, b in refs)
+    shape = dit.make_shape(1, n_txt, grid[0] * grid[1], nref)
+    ids = dit.dit_token_ids(shape, grid[0], grid[1], refs)
+    N = ids.shape[0]
+    table = torch.empty((N, 64, 2), dtype=torch.float32, device=DEV)
+    dit.dit_rope_table(dit.dit_config_klein(), ids.to(DEV), N, table)
+    torch.cuda.synchronize()
+    c, s = O.rope_table(O.token_ids(n_txt, grid[0], grid[1], refs))
+    t = table.cpu().numpy().astype(np.float64)
+    # fp64 angle rounded once to fp32
+    np.testing.assert_allclose(t[..., 0], c, rtol=0, atol=1.2e-7)
+    np.testing.assert_allclose(t[..., 1], s, rtol=0, atol=1.2e-7)
+
+
+@pytest.mark.parametrize("hidden,rows,split,batch", [(256, 96, 32, 1), (3072, 300, 77, 2), (3072, 4608, 512, 1)])
+def test_adaln(dit, hidden, rows, split, batch):
+    x_rows = rows + 5
+    x = _randn((batch, x_rows, hidden), 1.5, seed=1, mean=0.3).to(DEV)
+    mod = _randn((batch, 4, hidden), 0.1, seed=2).to(DEV)
+    y = torch.empty((batch, rows, hidden), dtype=torch.bfloat16, device=DEV)
+    dit.dit_adaln(batch, rows, hidden, x, x_rows, 3, split, mod[:, 0], mod[:, 1], mod[:, 2], mod[:, 3],
+                  4 * hidden, 1e-6, y)
+    torch.cuda.synchronize()
+    xn, mn = Hx.to_np(x), Hx.to_np(mod)
+    want = np.empty((batch, rows, hidden))
+    for b in range(batch):
+        xs = xn[b, 3:3 + rows]
+        want[b, :split] = O.adaln(xs[:split], mn[b, 0], mn[b, 1], 1e-6)
+        want[b, split:] = O.adaln(xs[split:], mn[b, 2], mn[b, 3], 1e-6)
+    _cmp(y, want)
+
+
+@pytest.mark.parametrize("wd", [synth.TINY, synth.KLEIN])
+@pytest.mark.parametrize("batch", [1, 3])
+def test_modulation(dit, wd, batch, ws):
+    g = synth.generator(7)
+    mw = synth.mod_weights(wd, g)
+    w = dit.dit_weights()
+    w.cfg = dit.make_config(hidden=wd.hidden, heads=wd.heads, mlp_hidden=wd.mlp_hidden)
+    dev = {k: v.to(DEV) for k, v in mw.items()}
+    w.mod.t_in, w.mod.t_out, w.mod.mod = dev["t_in"].data_ptr(), dev["t_out"].data_ptr(), dev["mod"].data_ptr()
+    sigma = torch.tensor([0.93, 0.51, 0.0][:batch], dtype=torch.float32)
+    out = torch.empty((batch, 17 * wd.hidden), dtype=torch.bfloat16, device=DEV)
+    dit.dit_modulation(w, sigma.to(DEV), batch, out, ws, ws.numel())
+    _check_status(dit, ws)
+    want = O.modulation(sigma.numpy().astype(np.float64), Hx.to_np(mw["t_in"]), Hx.to_np(mw["t_out"]),
+                        Hx.to_np(mw["mod"]), O.Config(hidden=wd.hidden))
+    _cmp(out, want, atol=1e-2)
+
+
+@pytest.mark.parametrize("batch,rows,n,k", [(1, 128, 256, 64), (2, 300, 288, 320), (1, 1000, 768, 3072),
+                                            (3, 17, 128, 7680)])
+def test_linear_store(dit, batch, rows, n, k, ws):
+    a = _randn((batch, rows, k), 1.0, seed=3).to(DEV)
+    w = _randn((n, k), 0.05, seed=4).to(DEV)
+    ld = n + 32
+    out = torch.full((batch, rows, ld), 7.0, dtype=torch.bfloat16, device=DEV)
+    dit.dit_linear(batch, rows, n, k, a, w, out, ld, dit.DIT_EPI_STORE, None, 0, ws, ws.numel())
+    _check_status(dit, ws)
+    want = Hx.to_np(a) @ Hx.to_np(w).T
+    scale = np.abs(want).max()
+    _cmp(out[..., :n], want, atol=1e-2 * scale)
+    assert (out[..., n:] == 7.0).all()  # columns past n_out untouched
+
+
+@pytest.mark.parametrize("batch,rows,n,k", [(1, 256, 256, 256), (2, 300, 3072, 320)])
+def test_linear_gated_residual(dit, batch, rows, n, k, ws):
+    a = _randn((batch, rows, k), 1.0, seed=5).to(DEV)
+    w = _randn((n, k), 0.05, seed=6).to(DEV)
+    x0 = _randn((batch, rows, n), 1.0, seed=7)
+    gate = _randn((batch, 3 * n), 0.1, seed=8)
+    x = x0.clone().to(DEV)
+    gd = gate.to(DEV)
+    dit.dit_linear(batch, rows, n, k, a, w, x, n, dit.DIT_EPI_GATED_RESIDUAL, gd[:, n:], 3 * n, ws, ws.numel())
+    _check_status(dit, ws)
+    want = Hx.to_np(x0) + Hx.to_np(gate)[:, None, n:2 * n] * (Hx.to_np(a) @ Hx.to_np(w).T)
+    _cmp(x, want)
+
+
+@pytest.mark.parametrize("batch,rows,f,k", [(1, 128, 128, 64), (2, 300, 768, 256), (1, 520, 9216, 3072)])
+def test_linear_swiglu_packed(dit, batch, rows, f, k, ws):
+    a = _randn((batch, rows, k), 1.0, seed=9).to(DEV)
+    w = _randn((2 * f, k), 0.05, seed=10)
+    wp = torch.empty((2 * f, k), dtype=torch.bfloat16, device=DEV)
+    dit.dit_pack_mlp_in(w.to(DEV), wp, f, k)
+    out = torch.zeros((batch, rows, f), dtype=torch.bfloat16, device=DEV)
+    dit.dit_linear(batch, rows, f, k, a, wp, out, f, dit.DIT_EPI_SWIGLU, None, 0, ws, ws.numel())
+    _check_status(dit, ws)
+    h = Hx.to_np(a) @ Hx.to_np(w).T
+    want = O.swiglu(h[..., :f], h[..., f:])
+    _cmp(out, want, atol=1e-2 * max(1.0, np.abs(want).max()))
+
+
+@pytest.mark.parametrize("batch,heads,n,qscale", [(1, 1, 128, 1.0), (1, 2, 300, 1.0), (2, 3, 1000, 1.0),
+                                                  (1, 2, 700, 6.0), (1, 1, 5, 1.0)])
+def test_attention(dit, batch, heads, n, qscale, ws):
+    q = _randn((batch, heads, n, 128), qscale, seed=11)
+    k = _randn((batch, heads, n, 128), 1.0, seed=12)
+    v = _randn((batch, heads, n, 128), 1.0, seed=13)
+    ld = heads * 128 + 64
+    out = torch.zeros((batch, n, ld), dtype=torch.bfloat16, device=DEV)
+    dit.dit_attention(batch, heads, n, q.to(DEV), k.to(DEV), v.to(DEV), out, ld, ws, ws.numel())
+    _check_status(dit, ws)
+    t = lambda z: Hx.to_np(z).transpose(0, 2, 1, 3)  # [B, N, heads, D]
+    want = O.attention(t(q), t(k), t(v)).reshape(batch, n, heads * 128)
+    _cmp(out[..., :heads * 128], want, atol=3e-2, cos_min=0.999)
+    assert (out[..., heads * 128:] == 0).all()
