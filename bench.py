@@ -153,6 +153,23 @@ def gpu_id_for_smi(torch, dev_index):
         return dev_index
 
 
+# ---------------------------------------------------------------------------------- ranks
+def reduce_max(x: float, world: int, device) -> float:
+    """Max of a per-rank scalar over all ranks (identity at world size 1)."""
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_steps_per_s(ms_per_step_max: float, world: int) -> float:
+    """Every rank runs its own replica (its own batch rows): the job completes `world`
+    steps in the slowest rank's step time."""
+    return world / (ms_per_step_max / 1e3)
+
+
 # ---------------------------------------------------------------------------------- CPU oracle
 def oracle_block_times(wl, seed=0, reps=1):
     """Seconds of one dual-stream and one single-stream block of the fp32 oracle at wl's shape."""
@@ -295,11 +312,8 @@ def run_ours(args, wl, rank, world, local_rank):
     st, where = dit.dit_sync_status(ws, stream)
     if st != dit.DIT_OK:
         raise RuntimeError(f"device wait gave up in the timed region at site {where:#x}")
-    ms = torch.tensor([ms_total], dtype=torch.float64, device=dev)
-    if world > 1:
-        tdist.all_reduce(ms, op=tdist.ReduceOp.MAX)
-    ms_step = ms.item() / args.steps
-    value = world * wl.batch / (ms_step / 1e3) / wl.batch  # steps/s, all replicas
+    ms_step = reduce_max(ms_total, world, dev) / args.steps
+    value = whole_job_steps_per_s(ms_step, world)
 
     # ---- e2e through the host-buffer entry point
     pin = lambda t: t.detach().to("cpu").contiguous().pin_memory() if t is not None else None
@@ -314,11 +328,7 @@ def run_ours(args, wl, rank, world, local_rank):
     for _ in range(k_e2e):
         dit.dit_step_host(W.w, shape, h_img, h_ref, h_txt, rope, h_sig, h_vel, ws, nbytes, stream)
         stream.synchronize()  # the caller reads the velocity every step
-    e2e_s = (time.perf_counter() - t0) / k_e2e
-    tt = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
-    if world > 1:
-        tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
-    e2e_s = tt.item()
+    e2e_s = reduce_max((time.perf_counter() - t0) / k_e2e, world, dev)
     h2d = sum(t.numel() * t.element_size() for t in (h_img, h_ref, h_txt, h_sig) if t is not None)
     d2h = h_vel.numel() * h_vel.element_size()
 
@@ -367,7 +377,7 @@ def run_ours(args, wl, rank, world, local_rank):
                                   "sustained": round(tflops / peak, 4), "nominal_2250": round(tflops / 2250.0, 4)},
             "roofline": roofline, "kernels": kernels,
             "cpu_baseline": cpu,
-            "e2e": {"value": round(world / e2e_s, 4), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "e2e": {"value": round(whole_job_steps_per_s(e2e_s * 1e3, world), 4), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": launches, "clocks": clocks}
     print(json.dumps(line), flush=True)

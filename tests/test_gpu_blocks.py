@@ -80,10 +80,14 @@ def run_block(dit, kind, wl, seed=0, check_rows=None):
         else:
             want = O.single_block(xin[b:b + 1], Hx.oracle_single(logical["single"][0], dt), mod_b, c, s, cfg, dt)
         err, cs = Hx.max_abs(got[b:b + 1], want), Hx.cosine(got[b:b + 1], want)
-        # the block's change to x is what it computed: check its direction too
-        dcs = Hx.cosine(got[b:b + 1] - xin[b:b + 1], want - xin[b:b + 1])
-        print(f"{kind} {wl.name} row {b}: max_abs {err:.4g} cos {cs:.7f} delta-cos {dcs:.6f}")
-        assert err <= BLOCK_ATOL and cs >= BLOCK_COS and dcs >= 0.99, (b, err, cs, dcs)
+        # The cosine above is dominated by the unchanged residual x; also check the block's
+        # own update x_out - x_in.  Its GPU value is quantised by the bf16 output, so it is
+        # compared with the oracle's output rounded to bf16 the same way.
+        want_q = torch.from_numpy(np.asarray(want, np.float32)).to(torch.bfloat16).float().numpy()
+        dcs = Hx.cosine(got[b:b + 1] - xin[b:b + 1], want_q - xin[b:b + 1])
+        print(f"{kind} {wl.name} row {b}: max_abs {err:.4g} cos {cs:.7f} update-cos {dcs:.6f}")
+        assert err <= BLOCK_ATOL and cs >= BLOCK_COS, (b, err, cs)
+        assert dcs >= 0.98, (b, dcs)
 
 
 @pytest.mark.parametrize("kind", ["dual", "single"])
@@ -177,6 +181,6 @@ def test_step_batch_invariance_ref_b4(dit):
     assert torch.isfinite(vel.float()).all()
     for b in (0, 3):
         wl1 = synth.Workload("row", wl.widths, 1, wl.n_txt, wl.grid, wl.ref_grids)
-        one = {k: (v[b:b + 1] if v is not None else None) for k, v in inp.items()}
+        one = {k: (v[b:b + 1].clone() if v is not None else None) for k, v in inp.items()}
         v1, _ = _step(dit, wl1, logical, one, W)
         assert torch.equal(v1[0], vel[b]), b
