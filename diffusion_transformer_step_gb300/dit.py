@@ -79,6 +79,7 @@ _SIGS = {
     "dit_adaln": (_I, [_I, _I, _I, _P, _I, _I, _I, _P, _P, _P, _P, _LL, _F, _P, _P]),
     "dit_linear": (_I, [_I, _I, _I, _I, _P, _P, _P, _I, _I, _P, _LL, _P, _SZ, _P]),
     "dit_attention": (_I, [_I, _I, _I, _P, _P, _P, _P, _I, _P, _SZ, _P]),
+    "dit_modulation_static": (_I, [C.POINTER(dit_weights), _P, _I, _P, _P]),
     "dit_launch_count": (C.c_ulonglong, []),
     "dit_timing_begin": (_I, [_I]),
     "dit_timing_end": (_I, [C.POINTER(_I), C.POINTER(_I), C.POINTER(_F), _I]),
@@ -238,6 +239,13 @@ def dit_linear(batch, rows, n_out, k, a_dev, w_dev, out_dev, ld_out, epi, gate_d
 def dit_attention(batch, heads, n, q_dev, k_dev, v_dev, out_dev, ld_out, ws, ws_bytes, stream=None):
     _check("dit_attention", lib().dit_attention(batch, heads, n, _ptr(q_dev), _ptr(k_dev), _ptr(v_dev), _ptr(out_dev),
                                                  ld_out, _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def dit_modulation_static(w: dit_weights, sigma_dev, batch: int, mod_dev, stream=None):
+    """dit_modulation without a workspace (scratch in a fixed device array of the library;
+    batch <= 8, hidden <= 4096), for callers that cannot allocate device memory."""
+    _check("dit_modulation_static", lib().dit_modulation_static(C.byref(w), _ptr(sigma_dev), batch, _ptr(mod_dev),
+                                                                 _stream(stream)))
 
 
 def dit_launch_count() -> int:

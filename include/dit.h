@@ -237,6 +237,25 @@ dit_status dit_linear(int batch, int rows, int n_out, int k, const void* a_dev, 
 dit_status dit_attention(int batch, int heads, int n, const void* q_dev, const void* k_dev, const void* v_dev,
                          void* out_dev, int ld_out, void* ws, size_t ws_bytes, dit_stream_t stream);
 
+/* ---- Allocation-free variant -------------------------------------------------------- */
+
+/* dit_modulation without a workspace, for callers that cannot allocate device memory
+ * where they run the modulation: a plugin inside a host framework that owns every device
+ * buffer and hands the plugin only its input and output tensors, or a serving loop that
+ * forbids allocation after start-up (cudaMalloc can synchronise the device and can fail
+ * once memory is fragmented).  The pages have no counterpart of this entry point; it
+ * computes what dit_modulation computes.  Its fp32 scratch (two [batch, hidden] vectors)
+ * lives in a fixed __device__ array of the library, 256 KB, which every GPU that loads the
+ * library holds until the process exits; so batch <= 8 and hidden <= 4096, and larger
+ * sizes return DIT_ERR_UNSUPPORTED with nothing launched.  The caller still passes
+ * sigma_dev [batch] fp32 and mod_dev [batch, 17H] bf16 (device).  The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress) with that device
+ * current: make that first call before any stream capture.  Every call shares the one
+ * array, so calls that overlap on the GPU (on different streams) race on it.  It never
+ * calls cudaMalloc, cudaFree or an allocating library routine. */
+dit_status dit_modulation_static(const dit_weights* w, const float* sigma_dev, int batch, void* mod_dev,
+                                 dit_stream_t stream);
+
 /* ---- Measurement ------------------------------------------------------------------ */
 
 /* Kernel launches issued by this library since it was loaded (all entry points). */
