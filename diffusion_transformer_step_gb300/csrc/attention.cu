@@ -3,19 +3,23 @@
 // text rows enter with no mask; reading R6 for the scale).  Padded tail keys of a tile
 // (sequence length not a multiple of 128) are masked out, padded tail queries not stored.
 //
-// One CTA per (128-query tile, head, batch row), 192 threads:
-//   warp 0      TMA: Q once; K_j and V_j tiles (128 keys x 128 dims, two 64-dim halves,
-//               128-byte swizzle) into a 2-stage ring, separate full/empty barriers for
-//               K and V so K_{j+2} streams in as soon as S_j is computed;
-//   warp 1      tcgen05.mma from one thread: S_j = Q K_j^T into one of two 128-column
-//               TMEM buffers, then O += P_{j-1} V_{j-1} (A = P from shared memory,
-//               K-major; B = V, MN-major) into a 128-column TMEM accumulator;
-//   warps 2-5   online softmax, one thread per query row: S row from TMEM, exp2 with
-//               the log2(e)/sqrt(d) scale folded in, P rounded to bf16 into shared memory
-//               (128-byte swizzled, the layout a TMA load would produce), O rescaled in
-//               TMEM only when the running maximum grows by more than 2^8 (the stale
-//               maximum keeps every P <= 256, exact after the final 1/l).
-// TMEM: S0 [0,128), S1 [128,256), O [256,384) of a 512-column allocation.
+// One CTA per (pair of 128-query tiles, head, batch row), 320 threads:
+//   warp 0      TMA: Q0, Q1 once; K_j and V_j (128 keys x 128 dims as two 64-dim halves,
+//               128-byte swizzle) into 2-stage rings with separate full/empty barriers;
+//   warp 1      tcgen05.mma from one thread, in the order
+//                 S0 = Q0 K_0^T, S1 = Q1 K_0^T, then for every key block j:
+//                 O0 += P0 V_j, S0 = Q0 K_{j+1}^T, O1 += P1 V_j, S1 = Q1 K_{j+1}^T,
+//               so that one tile's softmax overlaps the other tile's MMAs;
+//   warps 2-5   softmax of tile 0, warps 6-9 softmax of tile 1: one thread per query row,
+//               S row from TMEM, exp2 with log2(e)/sqrt(d) folded in, P rounded to bf16 and
+//               written back into TMEM over its own S, where the PV MMA reads it as its A
+//               operand; O rescaled in TMEM only when the running maximum grows by more
+//               than 2^8 (the stale maximum keeps every P <= 256; exact after the final 1/l).
+// Ordering: MMAs issued by one thread execute in order and a commit tracks every earlier
+// MMA of that thread, so "S_t of block j+1 is ready" also means "P_t V_j is complete":
+// the softmax may then rescale O_t and overwrite P_t without a further wait.
+// TMEM (512 columns): tile t uses S_t / P_t at [256t, 256t + 128) and O_t at
+// [256t + 128, 256t + 256).
 #include <math.h>
 
 #include "runtime.h"
@@ -25,14 +29,13 @@ namespace dit {
 namespace {
 
 constexpr int kBQ = 128, kBKV = 128;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr uint32_t kHalfBytes = 128 * 64 * 2;   // one 64-dim half of a 128-row tile
 constexpr uint32_t kTileBytes = 2 * kHalfBytes;  // 32 KB
-constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = kOffQ + kTileBytes;
+constexpr uint32_t kOffQ = 0;                    // Q0, Q1
+constexpr uint32_t kOffK = kOffQ + 2 * kTileBytes;
 constexpr uint32_t kOffV = kOffK + 2 * kTileBytes;
-constexpr uint32_t kOffP = kOffV + 2 * kTileBytes;
-constexpr uint32_t kOffBar = kOffP + kTileBytes;
+constexpr uint32_t kOffBar = kOffV + 2 * kTileBytes;
 constexpr size_t kSmemBytes = 1024 + kOffBar + 256;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -46,8 +49,9 @@ struct alignas(64) AttnParams {
 };
 
 enum : uint32_t {
-  kSiteQ = 0x201, kSiteKEmpty, kSiteVEmpty, kSiteKFull, kSiteSFree, kSitePFull, kSiteVFull, kSiteSFull, kSiteODone
+  kSiteQ = 0x201, kSiteKEmpty, kSiteVEmpty, kSiteKFull, kSitePFull, kSiteVFull, kSiteSFull, kSiteODone
 };
+
 
 __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_constant__ AttnParams P) {
   extern __shared__ uint8_t smem_raw[];
@@ -58,18 +62,17 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
   uint64_t* k_empty = bars + 3;  // [2]
   uint64_t* v_full = bars + 5;   // [2]
   uint64_t* v_empty = bars + 7;  // [2]
-  uint64_t* s_full = bars + 9;   // [2]
-  uint64_t* s_free = bars + 11;  // [2]
-  uint64_t* p_full = bars + 13;
-  uint64_t* o_done = bars + 14;
-  uint64_t* drain = bars + 15;
+  uint64_t* s_full = bars + 9;   // [2] per tile
+  uint64_t* p_full = bars + 11;  // [2] per tile
+  uint64_t* o_done = bars + 13;
+  uint64_t* drain = bars + 14;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n = P.n;
   const int nkv = (n + kBKV - 1) / kBKV;
-  const int q0 = blockIdx.x * kBQ;
+  const int q0 = blockIdx.x * (2 * kBQ);
   const int head = blockIdx.y, b = blockIdx.z;
   const int bh = b * P.heads + head;
 
@@ -81,9 +84,8 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 4);
+      mbar_init(&p_full[i], 4);
     }
-    mbar_init(p_full, 4);
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -107,11 +109,13 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      int pending_k = 0, pending_v = 0;  // loads issued whose completion was not observed
+      int pending_k = 0, pending_v = 0;
       bool ok = true;
-      mbar_arrive_expect_tx(q_full, kTileBytes);
-      tma_load_3d(smem + kOffQ, &P.q_map, q_full, 0, q0, bh);
-      tma_load_3d(smem + kOffQ + kHalfBytes, &P.q_map, q_full, 64, q0, bh);
+      mbar_arrive_expect_tx(q_full, 2 * kTileBytes);
+      for (int t = 0; t < 2; ++t) {
+        tma_load_3d(smem + kOffQ + t * kTileBytes, &P.q_map, q_full, 0, q0 + t * kBQ, bh);
+        tma_load_3d(smem + kOffQ + t * kTileBytes + kHalfBytes, &P.q_map, q_full, 64, q0 + t * kBQ, bh);
+      }
       for (int j = 0; j < nkv && ok; ++j) {
         const int st = j & 1;
         const uint32_t ph = (uint32_t)(j >> 1) & 1u;
@@ -150,47 +154,66 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
     if (lane == 0) {
       const uint32_t idesc_qk = make_idesc_bf16(128, 128, false);
       const uint32_t idesc_pv = make_idesc_bf16(128, 128, true);
-      const uint32_t sQ = smem_u32(smem + kOffQ);
-      const uint32_t sP = smem_u32(smem + kOffP);
-      const uint32_t tO = tmem + 256;
-      bool ok = mbar_wait(q_full, 0, wc, kSiteQ);
-      auto issue_pv = [&](int i) -> bool {
-        const int st = i & 1;
-        if (!mbar_wait(p_full, (uint32_t)i & 1u, wc, kSitePFull)) return false;
-        if (!mbar_wait(&v_full[st], (uint32_t)(i >> 1) & 1u, wc, kSiteVFull)) return false;
-        tc_fence_after();
-        const uint32_t sV = smem_u32(smem + kOffV + st * kTileBytes);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t ad = make_sdesc_sw128(sP + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = make_sdesc_sw128(sV + kk * 2048, kHalfBytes, 1024);
-          umma_bf16(tO, ad, bd, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(o_done);
-        umma_commit(&v_empty[st]);
-        return true;
-      };
-      for (int j = 0; j < nkv && ok; ++j) {
-        const int st = j & 1, sb = j & 1;
-        const uint32_t ph = (uint32_t)(j >> 1) & 1u;
-        if (!mbar_wait(&k_full[st], ph, wc, kSiteKFull) || !mbar_wait(&s_free[sb], ph ^ 1u, wc, kSiteSFree)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
+      auto issue_qk = [&](int t, int st) {
+        const uint32_t sQ = smem_u32(smem + kOffQ + t * kTileBytes);
         const uint32_t sK = smem_u32(smem + kOffK + st * kTileBytes);
-        const uint32_t tS = tmem + (uint32_t)(sb * 128);
+        const uint32_t tS = tmem + (uint32_t)(t * 256);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint64_t ad = make_sdesc_sw128(sQ + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
           const uint64_t bd = make_sdesc_sw128(sK + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
           umma_bf16(tS, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
         }
-        umma_commit(&s_full[sb]);
-        umma_commit(&k_empty[st]);
-        if (j > 0 && !issue_pv(j - 1)) ok = false;
+        umma_commit(&s_full[t]);
+      };
+      auto issue_pv = [&](int t, int st, bool acc) {
+        const uint32_t sV = smem_u32(smem + kOffV + st * kTileBytes);
+        const uint32_t tP = tmem + (uint32_t)(t * 256);
+        const uint32_t tO = tmem + (uint32_t)(t * 256 + 128);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t bd = make_sdesc_sw128(sV + kk * 2048, kHalfBytes, 1024);
+          umma_bf16_ts(tO, tP + kk * 8, bd, idesc_pv, (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = mbar_wait(q_full, 0, wc, kSiteQ) && mbar_wait(&k_full[0], 0, wc, kSiteKFull);
+      if (ok) {
+        tc_fence_after();
+        issue_qk(0, 0);
+        issue_qk(1, 0);
+        umma_commit(&k_empty[0]);
       }
-      if (ok) issue_pv(nkv - 1);
+      for (int j = 0; j < nkv && ok; ++j) {
+        const int st = j & 1, nst = (j + 1) & 1;
+        const bool more = j + 1 < nkv;
+        if (!mbar_wait(&v_full[st], (uint32_t)(j >> 1) & 1u, wc, kSiteVFull) ||
+            !mbar_wait(&p_full[0], (uint32_t)j & 1u, wc, kSitePFull)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_pv(0, st, j > 0);
+        if (more) {
+          if (!mbar_wait(&k_full[nst], (uint32_t)((j + 1) >> 1) & 1u, wc, kSiteKFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_qk(0, nst);
+        }
+        if (!mbar_wait(&p_full[1], (uint32_t)j & 1u, wc, kSitePFull)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_pv(1, st, j > 0);
+        umma_commit(&v_empty[st]);
+        if (more) {
+          issue_qk(1, nst);
+          umma_commit(&k_empty[nst]);
+        }
+      }
+      umma_commit(o_done);
       umma_commit(drain);
       const uint64_t t0 = global_timer_ns();
       while (!mbar_try(drain, 0) && global_timer_ns() - t0 < 1000000000ull) {
@@ -198,109 +221,100 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
     }
   } else {
     // ------------------------------------------------------------ softmax / correction / output
-    const int qq = warp & 3;
+    const int tile = (warp - 2) >> 2;  // warps 2-5 -> tile 0, warps 6-9 -> tile 1
+    const int qq = warp & 3;           // TMEM lane quarter of this warp
     const int row = qq * 32 + lane;
     const uint32_t lane_off = (uint32_t)(qq * 32) << 16;
-    const uint32_t tO = tmem + 256 + lane_off;
-    uint8_t* sP = smem + kOffP;
+    const uint32_t tS = tmem + (uint32_t)(tile * 256) + lane_off;
+    const uint32_t tO = tS + 128;
+    const float c = P.scale_log2;
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
-      const int sb = j & 1;
-      ok = mbar_wait(&s_full[sb], (uint32_t)(j >> 1) & 1u, wc, kSiteSFull);
+      ok = mbar_wait(&s_full[tile], (uint32_t)j & 1u, wc, kSiteSFull);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
       float s[128];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int cc = 0; cc < 4; ++cc) {
         uint32_t r[32];
-        tmem_load32(tmem + (uint32_t)(sb * 128 + c * 32) + lane_off, r);
+        tmem_load32(tS + cc * 32, r);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[i]);
+        for (int i = 0; i < 32; ++i) s[cc * 32 + i] = __uint_as_float(r[i]);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[sb]);
-
       const int kv_valid = n - j * kBKV;
       if (kv_valid < kBKV) {
 #pragma unroll
         for (int i = 0; i < 128; ++i)
           if (i >= kv_valid) s[i] = -INFINITY;
       }
-      float mx = -INFINITY;
+      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
-      for (int i = 0; i < 128; ++i) mx = fmaxf(mx, s[i]);
-      const float m_cand = fmaxf(m_run, mx * P.scale_log2);
+      for (int i = 4; i < 128; i += 4) {
+        mx0 = fmaxf(mx0, s[i]);
+        mx1 = fmaxf(mx1, s[i + 1]);
+        mx2 = fmaxf(mx2, s[i + 2]);
+        mx3 = fmaxf(mx3, s[i + 3]);
+      }
+      const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+      const float m_cand = fmaxf(m_run, mx * c);
       float alpha = 1.0f;
       bool resc = false;
       if (j == 0) {
         m_run = m_cand;
       } else if (m_cand > m_run + kRescaleThreshold) {
-        alpha = exp2f(m_run - m_cand);
+        alpha = ex2_approx(m_run - m_cand);
         m_run = m_cand;
         resc = true;
       }
-      float psum = 0.f;
-#pragma unroll
-      for (int i = 0; i < 128; ++i) {
-        s[i] = exp2f(fmaf(s[i], P.scale_log2, -m_run));
-        psum += s[i];
-      }
-      l_run = l_run * alpha + psum;
-
-      if (j > 0) {
-        bool ok2 = mbar_wait(o_done, (uint32_t)(j - 1) & 1u, wc, kSiteODone);
-        ok2 = __all_sync(0xffffffffu, ok2);
-        if (!ok2) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, resc)) {
+      // O_t already holds the sum over key blocks < j (P_t V_{j-1} completed before S_t
+      // of block j was signalled), so it may be rescaled now.
+      if (j > 0 && __any_sync(0xffffffffu, resc)) {
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            uint32_t r[32];
-            tmem_load32(tO + c * 32, r);
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t r[32];
+          tmem_load32(tO + cc * 32, r);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-            tmem_store32(tO + c * 32, r);
-          }
-          tmem_store_wait();
+          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+          tmem_store32(tO + cc * 32, r);
         }
       }
-      // P (bf16) into the 128-byte-swizzled K-major layout: half h holds keys
-      // [64h, 64h + 64); row r's 16-byte chunk c sits at chunk position c ^ (r & 7).
+      const float mneg = -m_run;
+      float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
-      for (int c8 = 0; c8 < 16; ++c8) {
-        const int half = c8 >> 3, chunk = c8 & 7;
-        uint4 v;
-        v.x = pack_bf16x2(s[c8 * 8 + 0], s[c8 * 8 + 1]);
-        v.y = pack_bf16x2(s[c8 * 8 + 2], s[c8 * 8 + 3]);
-        v.z = pack_bf16x2(s[c8 * 8 + 4], s[c8 * 8 + 5]);
-        v.w = pack_bf16x2(s[c8 * 8 + 6], s[c8 * 8 + 7]);
-        *reinterpret_cast<uint4*>(sP + half * kHalfBytes + row * 128 + ((chunk ^ (row & 7)) << 4)) = v;
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float p0 = ex2_approx(fmaf(s[h * 64 + 2 * i], c, mneg));
+          const float p1 = ex2_approx(fmaf(s[h * 64 + 2 * i + 1], c, mneg));
+          ps0 += p0;
+          ps1 += p1;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        tmem_store32(tS + h * 32, pk);  // P_t columns [32h, 32h + 32): keys [64h, 64h + 64)
       }
-      fence_proxy_async_smem();
+      l_run = l_run * alpha + (ps0 + ps1);
+      tmem_store_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
+      if (lane == 0) mbar_arrive(&p_full[tile]);
     }
     if (ok) {
-      bool ok2 = mbar_wait(o_done, (uint32_t)(nkv - 1) & 1u, wc, kSiteODone);
+      bool ok2 = mbar_wait(o_done, 0, wc, kSiteODone);
       ok2 = __all_sync(0xffffffffu, ok2);
       if (ok2) {
         tc_fence_after();
-        const int tok = q0 + row;
+        const int tok = q0 + tile * kBQ + row;
         const float inv_l = 1.0f / l_run;
         bf16* dst = P.out + ((long long)b * n + tok) * P.ld_out + head * 128;
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int cc = 0; cc < 4; ++cc) {
           uint32_t r[32];
-          tmem_load32(tO + c * 32, r);
+          tmem_load32(tO + cc * 32, r);
           if (tok < n) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+            uint4* d4 = reinterpret_cast<uint4*>(dst + cc * 32);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
               d4[i] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * i + 0]) * inv_l, __uint_as_float(r[8 * i + 1]) * inv_l),
@@ -350,7 +364,7 @@ cudaError_t launch_attention(int batch, int heads, int n, const bf16* q, const b
     if (e != cudaSuccess) return e;
     g_attr_set[dev] = true;
   }
-  dim3 grid((n + kBQ - 1) / kBQ, heads, batch);
+  dim3 grid((n + 2 * kBQ - 1) / (2 * kBQ), heads, batch);
   LaunchScope scope(kClsAttention, s);
   attention_kernel<<<grid, kThreads, kSmemBytes, s>>>(P);
   return cudaGetLastError();
