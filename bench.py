@@ -9,8 +9,9 @@ tokens, batch 1).  Prints ONE JSON line on rank 0.
 
   value      steps/s over the timed region, device-resident inputs (CUDA events on the
              launching stream, synchronised on both sides, max over ranks)
-  e2e        the same metric through dit_step_host: pinned host inputs copied in and the
-             velocity copied out inside the timed region
+  e2e        the same metric through dit_step_host (replayed from a CUDA graph): pinned host
+             inputs copied in and the velocity copied out inside the timed region, the host
+             waiting for every step's velocity
   roofline   the dominant kernel class (most device time in the timed region): its
              algorithmic FLOPs per launch / its mean launch time, measured live with CUDA
              events recorded around each launch on its own stream
@@ -319,20 +320,49 @@ def run_ours(args, wl, rank, world, local_rank):
     ms_step = reduce_max(ms_total, world, dev) / args.steps
     value = whole_job_steps_per_s(ms_step, world)
 
-    # ---- e2e through the host-buffer entry point
+    # ---- host cost of enqueueing one step (direct call, GPU idle before and after)
+    host_ms = []
+    for _ in range(3):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        step()
+        host_ms.append((time.perf_counter() - t0) * 1e3)
+    torch.cuda.synchronize()
+
+    # ---- the same step replayed from a CUDA graph (one enqueue per step)
+    g_dev = dit.dit_step_graph_create(W.w, shape, inp["img_tokens"], ref, inp["txt_emb"], rope, inp["sigma"], vel,
+                                      ws, nbytes, host_io=False, stream=stream)
+    for _ in range(2):
+        dit.dit_graph_launch(g_dev, stream)
+    barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        dit.dit_graph_launch(g_dev, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    graph_ms_step = reduce_max(e0.elapsed_time(e1), world, dev) / args.steps
+    dit.dit_graph_destroy(g_dev)
+
+    # ---- e2e through the host-buffer entry point (captured as a graph): every step copies
+    # its inputs from pinned host memory, runs, copies the velocity back, and the host waits
     pin = lambda t: t.detach().to("cpu").contiguous().pin_memory() if t is not None else None
     h_img, h_ref, h_txt, h_sig = pin(inp["img_tokens"]), pin(ref), pin(inp["txt_emb"]), pin(inp["sigma"])
     h_vel = torch.empty(tuple(vel.shape), dtype=torch.bfloat16).pin_memory()
-    for _ in range(max(1, args.warmup // 2)):
-        dit.dit_step_host(W.w, shape, h_img, h_ref, h_txt, rope, h_sig, h_vel, ws, nbytes, stream)
+    g_host = dit.dit_step_graph_create(W.w, shape, h_img, h_ref, h_txt, rope, h_sig, h_vel, ws, nbytes,
+                                       host_io=True, stream=stream)
+    for _ in range(2):
+        dit.dit_graph_launch(g_host, stream)
+        stream.synchronize()
     barrier()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     k_e2e = max(3, args.steps // 2)
     for _ in range(k_e2e):
-        dit.dit_step_host(W.w, shape, h_img, h_ref, h_txt, rope, h_sig, h_vel, ws, nbytes, stream)
+        dit.dit_graph_launch(g_host, stream)
         stream.synchronize()  # the caller reads the velocity every step
     e2e_s = reduce_max((time.perf_counter() - t0) / k_e2e, world, dev)
+    dit.dit_graph_destroy(g_host)
     h2d = sum(t.numel() * t.element_size() for t in (h_img, h_ref, h_txt, h_sig) if t is not None)
     d2h = h_vel.numel() * h_vel.element_size()
 
@@ -382,7 +412,10 @@ def run_ours(args, wl, rank, world, local_rank):
             "roofline": roofline, "kernels": kernels,
             "cpu_baseline": cpu,
             "e2e": {"value": round(whole_job_steps_per_s(e2e_s * 1e3, world), 4), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
+                    "d2h_bytes_per_step": d2h, "path": "dit_step_host captured in a CUDA graph, host sync every step"},
+            "graph_replay": {"value": round(whole_job_steps_per_s(graph_ms_step, world), 4), "unit": UNIT,
+                             "ms_per_step": round(graph_ms_step, 4)},
+            "host_enqueue_ms_per_step": round(min(host_ms), 3),
             "gpu_launches": launches, "clocks": clocks}
     print(json.dumps(line), flush=True)
 

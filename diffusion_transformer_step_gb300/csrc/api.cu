@@ -4,6 +4,7 @@
 #include <atomic>
 #include <cstring>
 #include <mutex>
+#include <new>
 #include <vector>
 
 #include "../../include/dit.h"
@@ -97,6 +98,7 @@ bool encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64
 namespace {
 
 constexpr int kMaxBatch = 64;
+constexpr int kMaxDenoiseSteps = 8;
 constexpr long long kMaxTokens = 1 << 20;
 
 inline bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -132,6 +134,7 @@ inline size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 struct Layout {
   size_t status, h1, h2, mod, x, x1, y, q, k, v, cat;
   size_t in_img, in_ref, in_txt, in_sigma, out_vel;
+  size_t den_sigma, den_coef, den_mod, den_h1, den_h2, den_state, den_xbf;
   size_t block_end, step_end, total;
 };
 
@@ -162,6 +165,13 @@ Layout layout(const dit_config& c, const dit_shape& s) {
   L.in_txt = take(B * (size_t)s.n_txt * c.txt_dim * 2);
   L.in_sigma = take(B * 4);
   L.out_vel = take(B * (size_t)s.n_img * c.in_channels * 2);
+  L.den_sigma = take((size_t)kMaxDenoiseSteps * B * 4);
+  L.den_coef = take((size_t)kMaxDenoiseSteps * B * 4);
+  L.den_mod = take((size_t)kMaxDenoiseSteps * B * 17 * H * 2);
+  L.den_h1 = take((size_t)kMaxDenoiseSteps * B * H * 4);
+  L.den_h2 = take((size_t)kMaxDenoiseSteps * B * H * 4);
+  L.den_state = take(B * (size_t)s.n_img * c.in_channels * 4);
+  L.den_xbf = take(B * (size_t)s.n_img * c.in_channels * 2);
   L.total = o;
   return L;
 }
@@ -316,6 +326,15 @@ dit_status run_single_block(const dit_weights* w, int layer, const dit_shape* s,
   return DIT_OK;
 }
 
+dit_status run_modulation_into(const dit_weights* w, const float* sigma, int batch, bf16* mod, float* h1, float* h2,
+                               cudaStream_t st) {
+  const int H = w->cfg.hidden;
+  DIT_CUDA(launch_timestep_in((const bf16*)w->mod.t_in, H, 256, sigma, batch, h1, st));
+  DIT_CUDA(launch_gemv((const bf16*)w->mod.t_out, H, H, h1, batch, 1, h2, nullptr, st));
+  DIT_CUDA(launch_gemv((const bf16*)w->mod.mod, 17 * H, H, h2, batch, 0, nullptr, mod, st));
+  return DIT_OK;
+}
+
 dit_status run_modulation(const dit_weights* w, const float* sigma, int batch, bf16* mod, void* ws,
                           const Layout& L, cudaStream_t st) {
   const int H = w->cfg.hidden;
@@ -347,17 +366,26 @@ dit_status check_step_weights(const dit_weights* w) {
   return DIT_OK;
 }
 
-dit_status run_step(const dit_weights* w, const dit_shape* s, const bf16* img, const bf16* ref, const bf16* txt,
-                    const float* rope, const float* sigma, bf16* vel, void* ws, cudaStream_t st) {
+// Where the final projection writes: the velocity (STORE), or, in the denoising loop, the
+// Euler update x_next = x + coef_b * v into an fp32 state and a bf16 copy.
+struct FinalOut {
+  bf16* vel;
+  const bf16* res_bf;
+  const float* res_f32;
+  const float* coef;
+  float* state;
+  bf16* out_bf;
+};
+
+dit_status run_step_core(const dit_weights* w, const dit_shape* s, const bf16* img, const bf16* ref,
+                         const bf16* txt, const float* rope, const bf16* mod, const FinalOut& fin, void* ws,
+                         cudaStream_t st) {
   const dit_config& c = w->cfg;
   const Layout L = layout(c, *s);
   const int B = s->batch, N = s->n_txt + s->n_img + s->n_ref, H = c.hidden, C = c.in_channels;
-  bf16* mod = bat(ws, L.mod);
   bf16* x = bat(ws, L.x);
   bf16* y = bat(ws, L.y);
   DeviceStatus* dst = status_of(ws);
-
-  DIT_TRY(run_modulation(w, sigma, B, mod, ws, L, st));
 
   // Embedders: text rows by ctx_emb, target-image rows by x_emb, into one [B, N, H].
   GemmProblemHost p[2];
@@ -390,10 +418,30 @@ dit_status run_step(const dit_weights* w, const dit_shape* s, const bf16* img, c
   DIT_CUDA(launch_adaln(af, st));
   p[0] = blank_problem();
   p[0].a = y; p[0].a_rows_total = s->n_img; p[0].lda = H; p[0].rows = s->n_img;
-  p[0].w = (const bf16*)w->proj_out; p[0].n = C; p[0].k = H; p[0].epi = kEpiStore;
-  p[0].out = vel; p[0].out_bstride = (long long)s->n_img * C; p[0].ld_out = C; p[0].out_row0 = 0;
+  p[0].w = (const bf16*)w->proj_out; p[0].n = C; p[0].k = H;
+  p[0].out_bstride = (long long)s->n_img * C; p[0].ld_out = C; p[0].out_row0 = 0;
+  if (fin.vel) {
+    p[0].epi = kEpiStore;
+    p[0].out = fin.vel;
+  } else {
+    p[0].epi = kEpiResidual;
+    p[0].res = fin.res_bf;
+    p[0].res_f32 = fin.res_f32;
+    p[0].coef = fin.coef;
+    p[0].out_f32 = fin.state;
+    p[0].out = fin.out_bf;
+  }
   DIT_CUDA(launch_gemm(p, 1, B, c.eps, dst, kClsGemmPlain, st));
   return DIT_OK;
+}
+
+dit_status run_step(const dit_weights* w, const dit_shape* s, const bf16* img, const bf16* ref, const bf16* txt,
+                    const float* rope, const float* sigma, bf16* vel, void* ws, cudaStream_t st) {
+  const Layout L = layout(w->cfg, *s);
+  bf16* mod = bat(ws, L.mod);
+  DIT_TRY(run_modulation(w, sigma, s->batch, mod, ws, L, st));
+  FinalOut fin{vel, nullptr, nullptr, nullptr, nullptr, nullptr};
+  return run_step_core(w, s, img, ref, txt, rope, mod, fin, ws, st);
 }
 
 }  // namespace
@@ -537,6 +585,47 @@ dit_status dit_step_fwd(const dit_weights* w, const dit_shape* shape, const void
                   sigma_dev, (bf16*)velocity_out, ws, (cudaStream_t)stream);
 }
 
+dit_status dit_denoise_fwd(const dit_weights* w, const dit_shape* shape, void* x_tokens, const void* ref_tokens,
+                           const void* txt_emb, const float* rope_dev, const float* sigmas_host, int steps, void* ws,
+                           size_t ws_bytes, dit_stream_t stream) {
+  DIT_TRY(check_step_weights(w));
+  DIT_TRY(check_shape(shape));
+  if (!aligned16(x_tokens) || !aligned16(txt_emb) || !aligned16(rope_dev) || !aligned16(ws) || !sigmas_host)
+    return DIT_ERR_INVALID_ARG;
+  if ((shape->n_ref > 0) != (ref_tokens != nullptr)) return DIT_ERR_INVALID_ARG;
+  if (ref_tokens && !aligned16(ref_tokens)) return DIT_ERR_INVALID_ARG;
+  if (steps < 1 || steps > kMaxDenoiseSteps) return DIT_ERR_INVALID_ARG;
+  for (int k = 0; k <= steps; ++k)
+    if (!(sigmas_host[k] >= 0.f && sigmas_host[k] <= 1000.f)) return DIT_ERR_INVALID_ARG;
+  const Layout L = layout(w->cfg, *shape);
+  if (ws_bytes < L.total) return DIT_ERR_WORKSPACE;
+  const cudaStream_t st = (cudaStream_t)stream;
+  const int B = shape->batch, H = w->cfg.hidden;
+  float* sig = reinterpret_cast<float*>(at(ws, L.den_sigma));
+  float* coef = reinterpret_cast<float*>(at(ws, L.den_coef));
+  bf16* mod = bat(ws, L.den_mod);
+  DIT_CUDA(launch_denoise_setup(sigmas_host, steps, B, sig, coef, st));
+  // The modulation of every step at once: rows k*B + b, at most 8 rows per weight pass.
+  const int rows = steps * B;
+  for (int r0 = 0; r0 < rows; r0 += 8) {
+    const int nr = rows - r0 < 8 ? rows - r0 : 8;
+    DIT_TRY(run_modulation_into(w, sig + r0, nr, mod + (long long)r0 * 17 * H,
+                                reinterpret_cast<float*>(at(ws, L.den_h1)), reinterpret_cast<float*>(at(ws, L.den_h2)),
+                                st));
+  }
+  bf16* xt = (bf16*)x_tokens;
+  bf16* xbf = bat(ws, L.den_xbf);
+  float* state = reinterpret_cast<float*>(at(ws, L.den_state));
+  for (int k = 0; k < steps; ++k) {
+    const bool first = k == 0, last = k == steps - 1;
+    FinalOut fin{nullptr, first ? xt : nullptr, first ? nullptr : state, coef + (long long)k * B, state,
+                 last ? xt : xbf};
+    DIT_TRY(run_step_core(w, shape, first ? xt : xbf, (const bf16*)ref_tokens, (const bf16*)txt_emb, rope_dev,
+                          mod + (long long)k * B * 17 * H, fin, ws, st));
+  }
+  return DIT_OK;
+}
+
 dit_status dit_step_host(const dit_weights* w, const dit_shape* shape, const void* img_tokens_host,
                          const void* ref_tokens_host, const void* txt_emb_host, const float* rope_dev,
                          const float* sigma_host, void* velocity_host, void* ws, size_t ws_bytes,
@@ -559,6 +648,84 @@ dit_status dit_step_host(const dit_weights* w, const dit_shape* shape, const voi
   DIT_TRY(run_step(w, shape, bat(ws, L.in_img), ref_b ? bat(ws, L.in_ref) : nullptr, bat(ws, L.in_txt), rope_dev,
                    reinterpret_cast<const float*>(at(ws, L.in_sigma)), bat(ws, L.out_vel), ws, st));
   DIT_CUDA(cudaMemcpyAsync(velocity_host, at(ws, L.out_vel), img_b, cudaMemcpyDeviceToHost, st));
+  return DIT_OK;
+}
+
+}  // extern "C"
+
+struct dit_graph_s {
+  cudaGraph_t graph;
+  cudaGraphExec_t exec;
+  unsigned long long kernels;  // kernel launches one replay performs
+};
+
+extern "C" {
+
+dit_status dit_step_graph_create(const dit_weights* w, const dit_shape* shape, const void* img_tokens,
+                                 const void* ref_tokens, const void* txt_emb, const float* rope_dev,
+                                 const float* sigma, void* velocity_out, void* ws, size_t ws_bytes, int host_io,
+                                 dit_stream_t stream, dit_graph* graph_out) {
+  if (!graph_out) return DIT_ERR_INVALID_ARG;
+  *graph_out = nullptr;
+  const cudaStream_t st = (cudaStream_t)stream;
+  auto enqueue = [&](dit_stream_t on) -> dit_status {
+    return host_io ? dit_step_host(w, shape, img_tokens, ref_tokens, txt_emb, rope_dev, sigma, velocity_out, ws,
+                                   ws_bytes, on)
+                   : dit_step_fwd(w, shape, img_tokens, ref_tokens, txt_emb, rope_dev, sigma, velocity_out, ws,
+                                  ws_bytes, on);
+  };
+  // Warm-up: validates every argument and performs the one-time per-kernel set-up
+  // (shared-memory attributes) outside the capture.
+  DIT_TRY(enqueue(stream));
+  DIT_CUDA(cudaStreamSynchronize(st));
+  // Capture on a private stream: the caller's may be the legacy default stream, which
+  // cannot be captured.  The graph is replayed on any stream later.
+  cudaStream_t cap = nullptr;
+  DIT_CUDA(cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking));
+  cudaGraph_t g = nullptr;
+  cudaError_t ce = cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal);
+  const unsigned long long before = g_launches.load();
+  dit_status es = DIT_OK;
+  if (ce == cudaSuccess) {
+    es = enqueue((dit_stream_t)cap);
+    ce = cudaStreamEndCapture(cap, &g);
+  }
+  // Captured launches did not run: count them when the graph is replayed instead.
+  const unsigned long long kernels = g_launches.load() - before;
+  g_launches.fetch_sub(kernels);
+  cudaStreamDestroy(cap);
+  if (es != DIT_OK || ce != cudaSuccess) {
+    if (g) cudaGraphDestroy(g);
+    cudaGetLastError();  // do not leave this failure for the next launch check to find
+    return es != DIT_OK ? es : DIT_ERR_CUDA;
+  }
+  cudaGraphExec_t exec = nullptr;
+  if (cudaGraphInstantiate(&exec, g, 0) != cudaSuccess) {
+    cudaGraphDestroy(g);
+    cudaGetLastError();
+    return DIT_ERR_CUDA;
+  }
+  dit_graph h = new (std::nothrow) dit_graph_s{g, exec, kernels};
+  if (!h) {
+    cudaGraphExecDestroy(exec);
+    cudaGraphDestroy(g);
+    return DIT_ERR_CUDA;
+  }
+  *graph_out = h;
+  return DIT_OK;
+}
+
+dit_status dit_graph_launch(dit_graph graph, dit_stream_t stream) {
+  if (!graph) return DIT_ERR_INVALID_ARG;
+  g_launches.fetch_add(graph->kernels, std::memory_order_relaxed);
+  return cuda_status(cudaGraphLaunch(graph->exec, (cudaStream_t)stream));
+}
+
+dit_status dit_graph_destroy(dit_graph graph) {
+  if (!graph) return DIT_OK;
+  cudaGraphExecDestroy(graph->exec);
+  cudaGraphDestroy(graph->graph);
+  delete graph;
   return DIT_OK;
 }
 

@@ -17,7 +17,9 @@
 // Epilogues (the fused block maths):
 //   STORE     bf16(acc)
 //   RESIDUAL  out <- x + gate * acc  (gated residual, reading R4); x and out bf16 or
-//             fp32, possibly the same buffer
+//             fp32 (or both outputs), possibly the same buffer; the gate is a bf16 vector
+//             per batch row, or one fp32 scalar per batch row (the Euler update
+//             x + (sigma_next - sigma) v of the denoising loop)
 //   SWIGLU    silu(acc[gate cols]) * acc[up cols]          (reading R9; packed W rows)
 //   QKV       columns [0, 3H): per-head RMSNorm (fp32, eps) * w, RoPE on adjacent pairs
 //             from the fp32 table, written head-major [B, heads, seq, 128]; columns
@@ -47,6 +49,7 @@ struct DevProblem {
   int ld_out, out_row0, out_col0;
   const bf16* gate;
   long long gate_stride;
+  const float* coef;
   int n_qkv, hidden;
   bf16 *q, *kk, *v;
   const bf16 *q_norm, *k_norm;
@@ -345,6 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         const long long off = (long long)ti.b * pr.out_bstride + (long long)(pr.out_row0 + r) * pr.ld_out +
                               pr.out_col0 + col0;
         const bf16* grow = pr.gate ? pr.gate + (long long)ti.b * pr.gate_stride + col0 : nullptr;
+        const float gsc = pr.coef ? pr.coef[ti.b] : 0.f;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t v[32];
@@ -355,14 +359,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
               float xr[32];
               if (pr.res_f32) load_row32_f32(pr.res_f32 + off + c * 32, xr);
               else load_row32(pr.res + off + c * 32, xr);
+              if (pr.coef) {
 #pragma unroll
-              for (int i = 0; i < 32; ++i) o[i] = xr[i] + __bfloat162float(grow[c * 32 + i]) * __uint_as_float(v[i]);
+                for (int i = 0; i < 32; ++i) o[i] = xr[i] + gsc * __uint_as_float(v[i]);
+              } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  o[i] = xr[i] + __bfloat162float(grow[c * 32 + i]) * __uint_as_float(v[i]);
+              }
             } else {
 #pragma unroll
               for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(v[i]);
             }
             if (pr.out_f32) store_row32_f32(pr.out_f32 + off + c * 32, o);
-            else store_row32(pr.out + off + c * 32, o);
+            if (pr.out) store_row32(pr.out + off + c * 32, o);
           }
         }
       } else if (pr.epi == kEpiSwiGLU || (pr.epi == kEpiQKV && col0 >= pr.n_qkv)) {
@@ -412,7 +422,27 @@ cudaError_t launch_gemm(const GemmProblemHost* probs, int nprob, int batch, floa
   for (int i = 0; i < nprob; ++i) {
     const GemmProblemHost& h = probs[i];
     DevProblem& d = P.prob[i];
-    if (h.rows <= 0 || h.n <= 0 || h.k <= 0) return cudaErrorInvalidValue;
+    if (h.rows <= 0 || h.n <= 0 || h.k <= 0 || !h.a || !h.w) return cudaErrorInvalidValue;
+    // every pointer the chosen epilogue dereferences must be present
+    switch (h.epi) {
+      case kEpiStore:
+        if (!h.out) return cudaErrorInvalidValue;
+        break;
+      case kEpiResidual:
+        if ((!h.gate && !h.coef) || (!h.out && !h.out_f32) || (!h.res && !h.res_f32 && !h.out))
+          return cudaErrorInvalidValue;
+        break;
+      case kEpiSwiGLU:
+        if (!h.out) return cudaErrorInvalidValue;
+        break;
+      case kEpiQKV:
+        if (!h.q || !h.kk || !h.v || !h.q_norm || !h.k_norm || !h.rope || h.hidden <= 0 ||
+            (h.n > h.n_qkv && !h.out))
+          return cudaErrorInvalidValue;
+        break;
+      default:
+        return cudaErrorInvalidValue;
+    }
     const uint64_t adims[3] = {(uint64_t)h.k, (uint64_t)h.a_rows_total, (uint64_t)batch};
     const uint64_t astr[2] = {(uint64_t)h.lda * 2, (uint64_t)h.lda * 2 * (uint64_t)h.a_rows_total};
     const uint32_t abox[3] = {BK, BM, 1};
@@ -440,6 +470,7 @@ cudaError_t launch_gemm(const GemmProblemHost* probs, int nprob, int batch, floa
     d.out_col0 = h.out_col0;
     d.gate = h.gate;
     d.gate_stride = h.gate_stride;
+    d.coef = h.coef;
     d.n_qkv = h.n_qkv;
     d.hidden = h.hidden;
     d.q = h.q;

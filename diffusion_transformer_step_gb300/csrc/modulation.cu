@@ -90,6 +90,19 @@ __global__ void __launch_bounds__(kWarps * 32) timestep_in_kernel(const bf16* __
   }
 }
 
+struct SigmaList {
+  float v[9];
+};
+
+__global__ void denoise_setup_kernel(SigmaList sl, int steps, int batch, float* __restrict__ sigma,
+                                     float* __restrict__ coef) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= steps * batch) return;
+  const int k = i / batch;
+  sigma[i] = sl.v[k];
+  coef[i] = sl.v[k + 1] - sl.v[k];
+}
+
 template <int NB>
 cudaError_t gemv_nb(const bf16* W, int n, int k, const float* x, int act, float* y_f32, bf16* y_bf16, int y_stride,
                     cudaStream_t s) {
@@ -129,6 +142,17 @@ cudaError_t launch_gemv(const bf16* W, int n, int k, const float* x, int batch, 
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+cudaError_t launch_denoise_setup(const float* sigmas_host, int steps, int batch, float* sigma, float* coef,
+                                 cudaStream_t s) {
+  if (steps < 1 || steps > 8) return cudaErrorInvalidValue;
+  SigmaList sl;
+  for (int k = 0; k <= steps; ++k) sl.v[k] = sigmas_host[k];
+  const int n = steps * batch;
+  LaunchScope scope(kClsModulation, s);
+  denoise_setup_kernel<<<(n + 127) / 128, 128, 0, s>>>(sl, steps, batch, sigma, coef);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_timestep_in(const bf16* t_in, int H, int time_dim, const float* sigma, int batch, float* h,

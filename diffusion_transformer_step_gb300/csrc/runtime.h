@@ -77,6 +77,11 @@ cudaError_t launch_gemv(const bf16* W, int n, int k, const float* x, int batch, 
 cudaError_t launch_timestep_in(const bf16* t_in, int H, int time_dim, const float* sigma, int batch, float* h,
                                cudaStream_t s);
 
+// Denoising loop set-up: sigma[k*B + b] = sigmas[k], coef[k*B + b] = sigmas[k+1] - sigmas[k]
+// for k < steps (sigmas: steps + 1 host values, steps <= 8).
+cudaError_t launch_denoise_setup(const float* sigmas_host, int steps, int batch, float* sigma, float* coef,
+                                 cudaStream_t s);
+
 cudaError_t launch_rope_table(const int32_t* ids, int n, const int* axes_dim, float theta, float* table,
                               cudaStream_t s);
 cudaError_t launch_pack_mlp_in(const bf16* src, bf16* dst, int F, int cols, cudaStream_t s);
@@ -99,7 +104,8 @@ struct GemmProblemHost {
   int n, k;
   int epi;
   // STORE / RESIDUAL / SWIGLU destination: out + b*out_bstride + (out_row0 + r)*ld_out
-  // + out_col0 + col.  RESIDUAL may write fp32 instead (out_f32, same addressing).
+  // + out_col0 + col.  RESIDUAL may write fp32 (out_f32, same addressing) instead of, or
+  // as well as, bf16.
   bf16* out;
   float* out_f32;
   // RESIDUAL input x (same addressing as out): bf16 res or fp32 res_f32; may alias out.
@@ -107,9 +113,11 @@ struct GemmProblemHost {
   const float* res_f32;
   long long out_bstride;
   int ld_out, out_row0, out_col0;
-  // RESIDUAL gate vector (n entries at gate + b*gate_stride).
+  // RESIDUAL gate vector (n entries at gate + b*gate_stride), or, when coef is set, one
+  // fp32 coefficient per batch row (coef[b]) for every column.
   const bf16* gate;
   long long gate_stride;
+  const float* coef;
   // QKV: columns [0, n_qkv) are q | k | v (each `hidden` wide); columns >= n_qkv are a
   // packed SwiGLU pair written to `out` at out_col0 + (col - n_qkv) / 2.
   int n_qkv, hidden;

@@ -74,12 +74,18 @@ _SIGS = {
     "dit_dual_block_fwd": (_I, [C.POINTER(dit_weights), _I, C.POINTER(dit_shape), _P, _P, _P, _P, _SZ, _P]),
     "dit_single_block_fwd": (_I, [C.POINTER(dit_weights), _I, C.POINTER(dit_shape), _P, _P, _P, _P, _SZ, _P]),
     "dit_step_fwd": (_I, [C.POINTER(dit_weights), C.POINTER(dit_shape), _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "dit_denoise_fwd": (_I, [C.POINTER(dit_weights), C.POINTER(dit_shape), _P, _P, _P, _P, C.POINTER(_F), _I, _P,
+                             _SZ, _P]),
     "dit_step_host": (_I, [C.POINTER(dit_weights), C.POINTER(dit_shape), _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "dit_sync_status": (_I, [_P, _P, C.POINTER(C.c_uint32)]),
     "dit_adaln": (_I, [_I, _I, _I, _P, _I, _I, _I, _P, _P, _P, _P, _LL, _F, _P, _P]),
     "dit_linear": (_I, [_I, _I, _I, _I, _P, _P, _P, _I, _I, _P, _LL, _P, _SZ, _P]),
     "dit_attention": (_I, [_I, _I, _I, _P, _P, _P, _P, _I, _P, _SZ, _P]),
     "dit_modulation_static": (_I, [C.POINTER(dit_weights), _P, _I, _P, _P]),
+    "dit_step_graph_create": (_I, [C.POINTER(dit_weights), C.POINTER(dit_shape), _P, _P, _P, _P, _P, _P, _P, _SZ,
+                                   _I, _P, C.POINTER(_P)]),
+    "dit_graph_launch": (_I, [_P, _P]),
+    "dit_graph_destroy": (_I, [_P]),
     "dit_launch_count": (C.c_ulonglong, []),
     "dit_timing_begin": (_I, [_I]),
     "dit_timing_end": (_I, [C.POINTER(_I), C.POINTER(_I), C.POINTER(_F), _I]),
@@ -206,12 +212,41 @@ def dit_step_fwd(w: dit_weights, shape: dit_shape, img_tokens, ref_tokens, txt_e
                                                _ptr(ws), ws_bytes, _stream(stream)))
 
 
+def dit_denoise_fwd(w: dit_weights, shape: dit_shape, x_tokens, ref_tokens, txt_emb, rope_dev, sigmas, ws,
+                    ws_bytes: int, stream=None):
+    """The steps-long Euler loop on the device, in place on x_tokens; `sigmas` is a host
+    sequence of steps + 1 floats."""
+    arr = (_F * len(sigmas))(*[float(v) for v in sigmas])
+    _check("dit_denoise_fwd", lib().dit_denoise_fwd(C.byref(w), C.byref(shape), _ptr(x_tokens), _ptr(ref_tokens),
+                                                     _ptr(txt_emb), _ptr(rope_dev), arr, len(sigmas) - 1, _ptr(ws),
+                                                     ws_bytes, _stream(stream)))
+
+
 def dit_step_host(w: dit_weights, shape: dit_shape, img_tokens_host, ref_tokens_host, txt_emb_host, rope_dev,
                   sigma_host, velocity_host, ws, ws_bytes: int, stream=None):
     _check("dit_step_host", lib().dit_step_host(C.byref(w), C.byref(shape), _ptr(img_tokens_host),
                                                  _ptr(ref_tokens_host), _ptr(txt_emb_host), _ptr(rope_dev),
                                                  _ptr(sigma_host), _ptr(velocity_host), _ptr(ws), ws_bytes,
                                                  _stream(stream)))
+
+
+def dit_step_graph_create(w: dit_weights, shape: dit_shape, img_tokens, ref_tokens, txt_emb, rope_dev, sigma,
+                          velocity_out, ws, ws_bytes: int, host_io: bool = False, stream=None) -> int:
+    """Capture one dit_step_fwd (host_io False) or dit_step_host (host_io True) call into a
+    CUDA graph; returns the opaque handle (an int)."""
+    h = _P()
+    _check("dit_step_graph_create", lib().dit_step_graph_create(
+        C.byref(w), C.byref(shape), _ptr(img_tokens), _ptr(ref_tokens), _ptr(txt_emb), _ptr(rope_dev), _ptr(sigma),
+        _ptr(velocity_out), _ptr(ws), ws_bytes, 1 if host_io else 0, _stream(stream), C.byref(h)))
+    return h.value
+
+
+def dit_graph_launch(graph: int, stream=None):
+    _check("dit_graph_launch", lib().dit_graph_launch(graph, _stream(stream)))
+
+
+def dit_graph_destroy(graph: int):
+    _check("dit_graph_destroy", lib().dit_graph_destroy(graph))
 
 
 def dit_sync_status(ws, stream=None):

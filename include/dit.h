@@ -190,6 +190,20 @@ dit_status dit_step_fwd(const dit_weights* w, const dit_shape* shape, const void
                         const void* ref_tokens, const void* txt_emb, const float* rope_dev, const float* sigma_dev,
                         void* velocity_out, void* ws, size_t ws_bytes, dit_stream_t stream);
 
+/* The denoising loop on the device ("flux2-klein-p100a" task table: steps fixed at 4, each
+ * one DiT call, guidance 1.0; "tt_flux2_klein -- Python reference", Lower-level entry
+ * points: denoise).  x_tokens [B, n_img, C] bf16 (device) holds the initial latent tokens
+ * and receives the final ones.  For k = 0 .. steps-1: v_k = the DiT step at sigma_k;
+ * x <- x + (sigma_{k+1} - sigma_k) v_k (flow-matching Euler update).  sigmas_host: steps + 1
+ * host floats in [0, 1000] (one schedule for every batch row; the 4-step klein schedule
+ * ends at 0), 1 <= steps <= 8.  The modulation of all steps is computed first in one pass
+ * over its weights; the latent is carried in fp32 in the workspace between steps and the
+ * Euler update runs in the final projection's epilogue.  Reference tokens and text
+ * features are the same at every step.  Workspace: dit_workspace_size bytes. */
+dit_status dit_denoise_fwd(const dit_weights* w, const dit_shape* shape, void* x_tokens, const void* ref_tokens,
+                           const void* txt_emb, const float* rope_dev, const float* sigmas_host, int steps, void* ws,
+                           size_t ws_bytes, dit_stream_t stream);
+
 /* dit_step_fwd with HOST inputs and output: copies img_tokens, ref_tokens, txt_emb and
  * sigma (host, same layouts; pinned memory gives asynchronous copies) into the
  * workspace, runs the step and copies the velocity back to velocity_host, all on
@@ -204,6 +218,29 @@ dit_status dit_step_host(const dit_weights* w, const dit_shape* shape, const voi
  * (or DIT_ERR_CUDA if the stream reports an error).  *where_out (may be NULL) receives
  * the id of the first wait that gave up. */
 dit_status dit_sync_status(void* ws, dit_stream_t stream, uint32_t* where_out);
+
+/* ---- CUDA graphs of a step (fixed shape and buffers) ------------------------------ */
+
+/* A captured, instantiated CUDA graph of one dit_step_fwd (host_io == 0) or one
+ * dit_step_host (host_io != 0) call with exactly these arguments: the same buffers are
+ * read and written on every launch (their contents may change between launches; for
+ * host_io the host buffers must be pinned).  Replaying it enqueues the whole step with one
+ * call instead of ~125, which matters when the caller synchronises after every step (the
+ * served path of the pages runs its compiled DiT inside CUDA-graph buckets for 1024², "FLUX.2
+ * [klein] 4B/9B + Z-Image-Turbo on a shared DiT scaffold", Known gaps).  Creation runs the
+ * step once on `stream` (warm-up), synchronises it, then captures; no other work may be
+ * enqueued on `stream` meanwhile.  The handle owns the graph; the buffers stay
+ * caller-owned and must outlive it.  Errors as for the step call, DIT_ERR_CUDA if capture
+ * or instantiation fails. */
+typedef struct dit_graph_s* dit_graph;
+dit_status dit_step_graph_create(const dit_weights* w, const dit_shape* shape, const void* img_tokens,
+                                 const void* ref_tokens, const void* txt_emb, const float* rope_dev,
+                                 const float* sigma, void* velocity_out, void* ws, size_t ws_bytes, int host_io,
+                                 dit_stream_t stream, dit_graph* graph_out);
+/* Enqueue one replay of the graph on `stream`. */
+dit_status dit_graph_launch(dit_graph graph, dit_stream_t stream);
+/* Release the graph (NULL is accepted). */
+dit_status dit_graph_destroy(dit_graph graph);
 
 /* ---- Component operations (the kernels a block is made of) ---------------------- */
 

@@ -184,3 +184,93 @@ def test_step_batch_invariance_ref_b4(dit):
         one = {k: (v[b:b + 1].clone() if v is not None else None) for k, v in inp.items()}
         v1, _ = _step(dit, wl1, logical, one, W)
         assert torch.equal(v1[0], vel[b]), b
+
+
+@pytest.mark.parametrize("host_io", [False, True])
+def test_step_graph_replay_matches_direct_call(dit, host_io):
+    """A captured step replays to the same bits as the direct call, also after the inputs
+    change between replays (the graph reads the buffers, not a snapshot)."""
+    wl = TINY_REF
+    logical = synth.model_weights(wl.widths, seed=6)
+    W = dit.DeviceWeights(wl.widths, logical)
+    shape, rope, ws, nbytes = _setup(dit, wl, W)
+    a, b = synth.step_inputs(wl, seed=6), synth.step_inputs(wl, seed=7)
+    loc = "cpu" if host_io else DEV
+    buf = {k: (v.to(loc).contiguous() if v is not None else None) for k, v in a.items()}
+    if host_io:
+        buf = {k: (v.pin_memory() if v is not None else None) for k, v in buf.items()}
+    out = torch.empty((wl.batch, wl.n_img, wl.widths.in_channels), dtype=torch.bfloat16, device=loc)
+    if host_io:
+        out = out.pin_memory()
+    g = dit.dit_step_graph_create(W.w, shape, buf["img_tokens"], buf["ref_tokens"], buf["txt_emb"], rope,
+                                  buf["sigma"], out, ws, nbytes, host_io=host_io)
+    try:
+        for inp in (a, b):
+            for k in buf:
+                if buf[k] is not None:
+                    buf[k].copy_(inp[k])
+            before = dit.dit_launch_count()
+            dit.dit_graph_launch(g)
+            _status(dit, ws)
+            # every kernel of the step is counted: modulation 3, embedders 1 (+1 with
+            # references), 7 per dual block, 4 per single block, final layer 2
+            wd = wl.widths
+            want_kernels = 3 + 1 + (1 if wl.n_ref else 0) + 7 * wd.n_dual + 4 * wd.n_single + 2
+            assert dit.dit_launch_count() - before == want_kernels
+            want, _ = _step(dit, wl, logical, inp, W)
+            assert torch.equal(out.to(DEV), want)
+    finally:
+        dit.dit_graph_destroy(g)
+
+
+def _schedule(inp):
+    # reading R19: 4 steps from the seeded sigma_0 down to 0; fp32 values fed to both sides
+    return O.sigma_schedule(float(inp["sigma"][0])).astype(np.float32)
+
+
+@pytest.mark.parametrize("wl", [synth.WORKLOADS["tiny"], TINY_REF], ids=lambda w: w.name)
+def test_denoise_loop_tiny(dit, wl):
+    """The 4-step loop on the device against the oracle's loop (fp64)."""
+    logical = synth.model_weights(wl.widths, seed=8)
+    inp = synth.step_inputs(wl, seed=8)
+    sig = _schedule(inp)
+    W = dit.DeviceWeights(wl.widths, logical)
+    shape, rope, ws, nbytes = _setup(dit, wl, W)
+    x = inp["img_tokens"].to(DEV).clone()
+    ref = inp["ref_tokens"].to(DEV) if inp["ref_tokens"] is not None else None
+    dit.dit_denoise_fwd(W.w, shape, x, ref, inp["txt_emb"].to(DEV), rope, sig.tolist(), ws, nbytes)
+    _status(dit, ws)
+    ow = Hx.oracle_weights(wl.widths, logical)
+    ids = O.token_ids(wl.n_txt, *wl.grid, wl.ref_grids)
+    x0 = Hx.to_np(inp["img_tokens"])
+    want = O.denoise(ow, x0, Hx.to_np(inp["ref_tokens"]), Hx.to_np(inp["txt_emb"]), ids, sig.astype(np.float64))
+    got = Hx.to_np(x)
+    cs, dcs = Hx.cosine(got, want), Hx.cosine(got - x0, want - x0)
+    print(f"denoise {wl.name}: cos {cs:.7f} displacement-cos {dcs:.6f} max_abs {Hx.max_abs(got, want):.4g}")
+    assert cs >= 0.999 and dcs >= STEP_COS
+
+
+def test_denoise_loop_matches_stepwise_klein_1024(dit):
+    """At the full 1024x1024 shape the device loop equals four dit_step_fwd calls with the
+    Euler update applied outside (fp32 latent, bf16 input to each step)."""
+    wl = synth.WORKLOADS["step_1024"]
+    logical = synth.model_weights(wl.widths, seed=9, device=DEV)
+    inp = synth.step_inputs(wl, seed=9, device=DEV)
+    sig = _schedule(inp)
+    W = dit.DeviceWeights(wl.widths, logical)
+    del logical
+    shape, rope, ws, nbytes = _setup(dit, wl, W)
+    x = inp["img_tokens"].clone()
+    dit.dit_denoise_fwd(W.w, shape, x, None, inp["txt_emb"], rope, sig.tolist(), ws, nbytes)
+    _status(dit, ws)
+    state = inp["img_tokens"].float()
+    vel = torch.empty_like(inp["img_tokens"])
+    for k in range(4):
+        sk = torch.full((1,), float(sig[k]), dtype=torch.float32, device=DEV)
+        dit.dit_step_fwd(W.w, shape, state.to(torch.bfloat16), None, inp["txt_emb"], rope, sk, vel, ws, nbytes)
+        state = state + (float(sig[k + 1]) - float(sig[k])) * vel.float()
+    _status(dit, ws)
+    want = state.to(torch.bfloat16)
+    d = Hx.cosine(Hx.to_np(x) - Hx.to_np(inp["img_tokens"]), Hx.to_np(want) - Hx.to_np(inp["img_tokens"]))
+    print(f"denoise step_1024 vs stepwise: displacement-cos {d:.6f}")
+    assert d >= 0.999
