@@ -11,10 +11,12 @@
 //                 O0 += P0 V_j, S0 = Q0 K_{j+1}^T, O1 += P1 V_j, S1 = Q1 K_{j+1}^T,
 //               so that one tile's softmax overlaps the other tile's MMAs;
 //   warps 2-5   softmax of tile 0, warps 6-9 softmax of tile 1: one thread per query row,
-//               S row from TMEM, exp2 with log2(e)/sqrt(d) folded in, P rounded to bf16 and
-//               written back into TMEM over its own S, where the PV MMA reads it as its A
-//               operand; O rescaled in TMEM only when the running maximum grows by more
-//               than 2^8 (the stale maximum keeps every P <= 256; exact after the final 1/l).
+//               S row streamed from TMEM in 32-key chunks, exp2 against the running
+//               maximum with log2(e)/sqrt(d) folded in, P rounded to bf16 and written back
+//               into TMEM over its own S, where the PV MMA reads it as its A operand.  The
+//               running maximum is lazy: it (and O, in TMEM) is updated only when a key
+//               exceeds it by more than 2^8, which keeps every P <= 256 and is exact after
+//               the final 1/l; only then (and on the first key block) is S read twice.
 // Ordering: MMAs issued by one thread execute in order and a commit tracks every earlier
 // MMA of that thread, so "S_t of block j+1 is ready" also means "P_t V_j is complete":
 // the softmax may then rescale O_t and overwrite P_t without a further wait.
@@ -48,10 +50,98 @@ struct alignas(64) AttnParams {
   DeviceStatus* status;
 };
 
+// ---- softmax arithmetic helpers -----------------------------------------------------
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// (d0, d1) = (a0, a1) * b + c with one packed fp32x2 FMA.
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b, float c) {
+  uint64_t A, B, C, D;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(A) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(B) : "f"(b));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(C) : "f"(c));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(D) : "l"(A), "l"(B), "l"(C));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(d0), "=f"(d1) : "l"(D));
+}
+
+// (s0, s1) += (a0, a1) with one packed fp32x2 add.
+__device__ __forceinline__ void fadd2(float& s0, float& s1, float a0, float a1) {
+  uint64_t S, A;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(S) : "f"(s0), "f"(s1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(A) : "f"(a0), "f"(a1));
+  asm("add.f32x2 %0, %0, %1;" : "+l"(S) : "l"(A));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(s0), "=f"(s1) : "l"(S));
+}
+
+// One 32-key chunk of a softmax row: running key maximum (raw scores), P = 2^(s c - m)
+// packed to bf16 pairs, and the two partial row sums; kTail: keys at or past kv_valid
+// masked to -inf.  Every exponential runs on MUFU: moving a share of them to an FMA-pipe
+// polynomial was measured slower here (the softmax is latency-, not MUFU-bound).
+template <bool kTail>
+__device__ __forceinline__ void softmax_chunk(const uint32_t (&r)[32], int base, int kv_valid, float c, float mneg,
+                                              float& smax, float& ps0, float& ps1, uint32_t* pk) {
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {
+    float s0 = __uint_as_float(r[i]), s1 = __uint_as_float(r[i + 1]);
+    if (kTail) {
+      if (base + i >= kv_valid) s0 = -INFINITY;
+      if (base + i + 1 >= kv_valid) s1 = -INFINITY;
+    }
+    smax = fmax3(smax, s0, s1);
+    float x0, x1;
+    ffma2(x0, x1, s0, s1, c, mneg);
+    const float p0 = ex2_approx(x0);
+    const float p1 = ex2_approx(x1);
+    fadd2(ps0, ps1, p0, p1);
+    pk[i / 2] = pack_bf16x2(p0, p1);
+  }
+}
+
+template <bool kTail>
+__device__ __forceinline__ void softmax_row(uint32_t tS, int kv_valid, float c, float mneg, float& smax, float& psum,
+                                            uint32_t (&pk)[64]) {
+  float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t r[32];
+    tmem_load32(tS + q * 32, r);
+    softmax_chunk<kTail>(r, q * 32, kv_valid, c, mneg, smax, ps0, ps1, &pk[q * 16]);
+  }
+  psum = ps0 + ps1;
+}
+
 enum : uint32_t {
   kSiteQ = 0x201, kSiteKEmpty, kSiteVEmpty, kSiteKFull, kSitePFull, kSiteVFull, kSiteSFull, kSiteODone
 };
 
+
+__device__ __forceinline__ void issue_qk(uint8_t* smem, uint32_t tmem, int t, int st, uint32_t idesc, uint64_t* bar) {
+  const uint32_t sQ = smem_u32(smem + kOffQ + t * kTileBytes);
+  const uint32_t sK = smem_u32(smem + kOffK + st * kTileBytes);
+  const uint32_t tS = tmem + (uint32_t)(t * 256);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint64_t ad = make_sdesc_sw128(sQ + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
+    const uint64_t bd = make_sdesc_sw128(sK + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
+    umma_bf16(tS, ad, bd, idesc, kk > 0 ? 1u : 0u);
+  }
+  umma_commit(bar);
+}
+
+__device__ __forceinline__ void issue_pv(uint8_t* smem, uint32_t tmem, int t, int st, bool acc, uint32_t idesc) {
+  const uint32_t sV = smem_u32(smem + kOffV + st * kTileBytes);
+  const uint32_t tP = tmem + (uint32_t)(t * 256);
+  const uint32_t tO = tmem + (uint32_t)(t * 256 + 128);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint64_t bd = make_sdesc_sw128(sV + kk * 2048, kHalfBytes, 1024);
+    umma_bf16_ts(tO, tP + kk * 8, bd, idesc, (acc || kk > 0) ? 1u : 0u);
+  }
+}
 
 __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_constant__ AttnParams P) {
   extern __shared__ uint8_t smem_raw[];
@@ -154,33 +244,11 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
     if (lane == 0) {
       const uint32_t idesc_qk = make_idesc_bf16(128, 128, false);
       const uint32_t idesc_pv = make_idesc_bf16(128, 128, true);
-      auto issue_qk = [&](int t, int st) {
-        const uint32_t sQ = smem_u32(smem + kOffQ + t * kTileBytes);
-        const uint32_t sK = smem_u32(smem + kOffK + st * kTileBytes);
-        const uint32_t tS = tmem + (uint32_t)(t * 256);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t ad = make_sdesc_sw128(sQ + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = make_sdesc_sw128(sK + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
-          umma_bf16(tS, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
-        }
-        umma_commit(&s_full[t]);
-      };
-      auto issue_pv = [&](int t, int st, bool acc) {
-        const uint32_t sV = smem_u32(smem + kOffV + st * kTileBytes);
-        const uint32_t tP = tmem + (uint32_t)(t * 256);
-        const uint32_t tO = tmem + (uint32_t)(t * 256 + 128);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t bd = make_sdesc_sw128(sV + kk * 2048, kHalfBytes, 1024);
-          umma_bf16_ts(tO, tP + kk * 8, bd, idesc_pv, (acc || kk > 0) ? 1u : 0u);
-        }
-      };
       bool ok = mbar_wait(q_full, 0, wc, kSiteQ) && mbar_wait(&k_full[0], 0, wc, kSiteKFull);
       if (ok) {
         tc_fence_after();
-        issue_qk(0, 0);
-        issue_qk(1, 0);
+        issue_qk(smem, tmem, 0, 0, idesc_qk, &s_full[0]);
+        issue_qk(smem, tmem, 1, 0, idesc_qk, &s_full[1]);
         umma_commit(&k_empty[0]);
       }
       for (int j = 0; j < nkv && ok; ++j) {
@@ -192,24 +260,24 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
           break;
         }
         tc_fence_after();
-        issue_pv(0, st, j > 0);
+        issue_pv(smem, tmem, 0, st, j > 0, idesc_pv);
         if (more) {
           if (!mbar_wait(&k_full[nst], (uint32_t)((j + 1) >> 1) & 1u, wc, kSiteKFull)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          issue_qk(0, nst);
+          issue_qk(smem, tmem, 0, nst, idesc_qk, &s_full[0]);
         }
         if (!mbar_wait(&p_full[1], (uint32_t)j & 1u, wc, kSitePFull)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        issue_pv(1, st, j > 0);
+        issue_pv(smem, tmem, 1, st, j > 0, idesc_pv);
         umma_commit(&v_empty[st]);
         if (more) {
-          issue_qk(1, nst);
+          issue_qk(smem, tmem, 1, nst, idesc_qk, &s_full[1]);
           umma_commit(&k_empty[nst]);
         }
       }
@@ -235,67 +303,63 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      float s[128];
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t r[32];
-        tmem_load32(tS + cc * 32, r);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[cc * 32 + i] = __uint_as_float(r[i]);
-      }
       const int kv_valid = n - j * kBKV;
-      if (kv_valid < kBKV) {
-#pragma unroll
-        for (int i = 0; i < 128; ++i)
-          if (i >= kv_valid) s[i] = -INFINITY;
+      // Fast path: exponentials against the running maximum, streamed over four
+      // 32-key chunks of S, only the packed P kept.  Valid unless some key exceeds the
+      // running maximum by more than 2^8 (and always wrong on the first key block).
+      uint32_t pk[64];
+      float psum = 0.f, smax = -INFINITY;
+      bool slow = (j == 0);
+      if (!slow) {
+        if (kv_valid >= kBKV)
+          softmax_row<false>(tS, kv_valid, c, -m_run, smax, psum, pk);
+        else
+          softmax_row<true>(tS, kv_valid, c, -m_run, smax, psum, pk);
+        slow = smax * c > m_run + kRescaleThreshold;
       }
-      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
-#pragma unroll
-      for (int i = 4; i < 128; i += 4) {
-        mx0 = fmaxf(mx0, s[i]);
-        mx1 = fmaxf(mx1, s[i + 1]);
-        mx2 = fmaxf(mx2, s[i + 2]);
-        mx3 = fmaxf(mx3, s[i + 3]);
-      }
-      const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
-      const float m_cand = fmaxf(m_run, mx * c);
       float alpha = 1.0f;
-      bool resc = false;
-      if (j == 0) {
-        m_run = m_cand;
-      } else if (m_cand > m_run + kRescaleThreshold) {
-        alpha = ex2_approx(m_run - m_cand);
-        m_run = m_cand;
-        resc = true;
-      }
-      // O_t already holds the sum over key blocks < j (P_t V_{j-1} completed before S_t
-      // of block j was signalled), so it may be rescaled now.
-      if (j > 0 && __any_sync(0xffffffffu, resc)) {
-#pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
+      if (__any_sync(0xffffffffu, slow)) {
+        // Slow path (whole warp): the block maximum first, then the exponentials again.
+        float mx = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
           uint32_t r[32];
-          tmem_load32(tO + cc * 32, r);
+          tmem_load32(tS + q * 32, r);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-          tmem_store32(tO + cc * 32, r);
+          for (int i = 0; i < 32; ++i)
+            if (kv_valid >= kBKV || q * 32 + i < kv_valid) mx = fmaxf(mx, __uint_as_float(r[i]));
         }
-      }
-      const float mneg = -m_run;
-      float ps0 = 0.f, ps1 = 0.f;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float p0 = ex2_approx(fmaf(s[h * 64 + 2 * i], c, mneg));
-          const float p1 = ex2_approx(fmaf(s[h * 64 + 2 * i + 1], c, mneg));
-          ps0 += p0;
-          ps1 += p1;
-          pk[i] = pack_bf16x2(p0, p1);
+        const float m_cand = fmaxf(m_run, mx * c);
+        bool resc = false;
+        if (j == 0) {
+          m_run = m_cand;
+        } else if (m_cand > m_run + kRescaleThreshold) {
+          alpha = ex2_approx(m_run - m_cand);
+          m_run = m_cand;
+          resc = true;
         }
-        tmem_store32(tS + h * 32, pk);  // P_t columns [32h, 32h + 32): keys [64h, 64h + 64)
+        // O_t holds the sum over key blocks < j (P_t V_{j-1} completed before S_t of
+        // block j was signalled), so it may be rescaled now.
+        if (j > 0 && __any_sync(0xffffffffu, resc)) {
+#pragma unroll 1
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t r[32];
+            tmem_load32(tO + cc * 32, r);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+            tmem_store32(tO + cc * 32, r);
+          }
+        }
+        float unused = -INFINITY;
+        if (kv_valid >= kBKV)
+          softmax_row<false>(tS, kv_valid, c, -m_run, unused, psum, pk);
+        else
+          softmax_row<true>(tS, kv_valid, c, -m_run, unused, psum, pk);
       }
-      l_run = l_run * alpha + (ps0 + ps1);
+      l_run = l_run * alpha + psum;
+      // P_t over S_t columns [0, 64): keys [2c, 2c + 1] in column c
+      tmem_store32(tS, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
+      tmem_store32(tS + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
       tmem_store_wait();
       tc_fence_before();
       __syncwarp();
