@@ -1,18 +1,24 @@
 // Persistent tcgen05 GEMM with fused epilogues: out = A W^T, A [rows, k] and W [n, k]
 // both K-major bf16, fp32 accumulation in Tensor Memory.
 //
-// One CTA per SM, 192 threads:
-//   warp 0      TMA producer: A tile 128 x 64 and W tile 256 x 64 per stage, 128-byte
-//               swizzle, 4-stage shared-memory ring guarded by full/empty mbarriers;
-//   warp 1      allocates 512 TMEM columns (two 128 x 256 fp32 accumulators) and issues
-//               tcgen05.mma (M=128, N=256, K=16) from one thread, committing each stage
-//               back to its empty barrier and each finished tile to an accumulator-full
-//               barrier;
-//   warps 2-5   epilogue: one thread per accumulator row, tcgen05.ld 32 columns at a
-//               time, fused math, 16-byte global stores; then hand the accumulator back.
+// CTA pairs (clusters of 2, tcgen05 cta_group::2), one CTA per SM, 192 threads each.  A
+// pair computes a 256 x 256 tile: CTA r loads rows [128r, 128r + 128) of the A tile and
+// rows [128r, 128r + 128) of the W tile, so each CTA streams 32 KB per 64-deep k-block
+// (a 1-CTA 128 x 256 tile needs 48 KB for half the work) and 6 stages fit in shared memory.
+//   warp 0      TMA producer in both CTAs: 128-byte-swizzled tiles into a 6-stage ring;
+//               both CTAs' loads complete on the leader CTA's full barrier, and the CTA
+//               owning the first M tile of a weight column prefetches that column's W tiles
+//               8 k-blocks ahead into L2 (one prefetcher per column, not every reader);
+//   warp 1      allocates 512 TMEM columns in both CTAs (two 128 x 256 fp32 accumulators
+//               per CTA) and, in the leader only, issues tcgen05.mma.cta_group::2 (M=256,
+//               N=256, K=16) from one thread; commits are multicast to both CTAs' empty
+//               and accumulator-full barriers;
+//   warps 2-5   epilogue in both CTAs: one thread per accumulator row of its own CTA,
+//               tcgen05.ld 32 columns at a time, fused math, 16-byte global stores; the
+//               accumulator is handed back on the leader's barrier (8 arrivals).
 // The two accumulators let tile i's epilogue overlap tile i+1's main loop.  Up to two
 // problems (the text and image streams of a dual-stream block) share one launch; tiles
-// are ordered with M fastest so that concurrent CTAs share the same weight slab in L2.
+// are ordered with M fastest so that concurrent pairs share the same weight slab in L2.
 //
 // Epilogues (the fused block maths):
 //   STORE     bf16(acc)
@@ -30,11 +36,12 @@ namespace dit {
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int kStages = 4;
+constexpr int BM = 128, BN = 256, BK = 64;   // per CTA: 128 rows of A; the pair's tile is 256 x 256
+constexpr int PAIR_M = 2 * BM;
+constexpr int kStages = 6;
 constexpr int kThreads = 192;
-constexpr uint32_t kATileBytes = BM * BK * 2;  // 16 KB
-constexpr uint32_t kBTileBytes = BN * BK * 2;  // 32 KB
+constexpr uint32_t kATileBytes = BM * BK * 2;        // 16 KB (this CTA's half of A)
+constexpr uint32_t kBTileBytes = (BN / 2) * BK * 2;  // 16 KB (this CTA's half of B)
 constexpr uint32_t kStageBytes = kATileBytes + kBTileBytes;
 constexpr uint32_t kTmemCols = 2 * BN;
 constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + 256;
@@ -85,6 +92,46 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& P, int t) {
 
 // Wait sites, reported through DeviceStatus::where.
 enum : uint32_t { kSiteEmpty = 0x101, kSiteFull = 0x102, kSiteAccEmpty = 0x103, kSiteAccFull = 0x104 };
+
+__device__ __forceinline__ uint32_t cta_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void arrive_cluster(uint32_t caddr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
+}
+__device__ __forceinline__ void tma3_2sm(void* dst, const CUtensorMap* m, uint32_t mbar_cluster, int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::
+          "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(m)), "r"(mbar_cluster), "r"(x), "r"(y), "r"(z) : "memory");
+}
+__device__ __forceinline__ void tma2_2sm(void* dst, const CUtensorMap* m, uint32_t mbar_cluster, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::
+          "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(m)), "r"(mbar_cluster), "r"(x), "r"(y) : "memory");
+}
+// Bring a weight tile into L2 ahead of its shared-memory load (no completion to wait for).
+__device__ __forceinline__ void pf_l2(const CUtensorMap* m, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(m)),
+               "r"(x), "r"(y) : "memory");
+}
+__device__ __forceinline__ void umma2(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t acc) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+               "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(acc) : "memory");
+}
+__device__ __forceinline__ void commit_both(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(smem_u32(bar)),
+               "h"((uint16_t)3) : "memory");
+}
 
 __device__ __forceinline__ void store_row32(bf16* dst, const float* f) {
   uint4* d = reinterpret_cast<uint4*>(dst);
@@ -196,7 +243,8 @@ __device__ __forceinline__ void epi_qkv_head(uint32_t tb, bool row_ok, int which
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmParams P) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ GemmParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -210,6 +258,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cta_rank();          // 0 = leader (issues the MMAs), 1 = peer
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
@@ -217,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], 4);
+      mbar_init(&acc_empty[a], 8);  // 4 epilogue warps in each CTA of the pair
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -230,35 +280,40 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     }
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, kTmemCols);
-    tmem_relinquish();
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(kTmemCols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();  // barriers of both CTAs initialised, TMEM allocated in both
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtx wc{P.status, abort_flag, kWaitLimitNs};
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
       long long issued = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < P.total_tiles && ok; t += gridDim.x) {
+      for (int t = pair; t < P.total_tiles && ok; t += npairs) {
         const TileInfo ti = decode_tile(P, t);
         const DevProblem& pr = P.prob[ti.p];
         const int kblocks = (pr.k + BK - 1) / BK;
-        const int arow = pr.a_row0 + ti.m_tile * BM;
-        const int brow = ti.n_tile * BN;
+        const int arow = pr.a_row0 + ti.m_tile * PAIR_M + (int)rank * BM;
+        const int brow = ti.n_tile * BN + (int)rank * (BN / 2);
+        const bool pf = ti.m_tile == 0;
         for (int kb = 0; kb < kblocks; ++kb) {
+          if (pf && kb + 8 < kblocks) pf_l2(&P.b_map[ti.p], (kb + 8) * BK, brow);
           if (!mbar_wait(&empty[stage], phase ^ 1u, wc, kSiteEmpty)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[stage], kStageBytes);
-          tma_load_3d(sA + stage * kATileBytes, &P.a_map[ti.p], &full[stage], kb * BK, arow, ti.b);
-          tma_load_2d(sB + stage * kBTileBytes, &P.b_map[ti.p], &full[stage], kb * BK, brow);
+          // both CTAs' loads complete on the leader's full barrier
+          const uint32_t fb = map_to_rank(smem_u32(&full[stage]), 0);
+          if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes);
+          tma3_2sm(sA + stage * kATileBytes, &P.a_map[ti.p], fb, kb * BK, arow, ti.b);
+          tma2_2sm(sB + stage * kBTileBytes, &P.b_map[ti.p], fb, kb * BK, brow);
           ++issued;
           if (++stage == kStages) {
             stage = 0;
@@ -266,8 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           }
         }
       }
-      if (!ok) {
-        // Unwinding: let the copies already issued land before the block exits.
+      if (!ok && rank == 0) {
         const long long outstanding = issued < kStages ? issued : kStages;
         for (long long i = 0; i < outstanding; ++i) {
           if (stage == 0) {
@@ -282,13 +336,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc = make_idesc_bf16(BM, BN, false);
+    // ------------------------------------------------------------ MMA issuer (leader only)
+    if (lane == 0 && rank == 0) {
+      const uint32_t idesc = make_idesc_bf16(PAIR_M, BN, false);
       uint32_t stage = 0, phase = 0;
       int local = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < P.total_tiles && ok; t += gridDim.x, ++local) {
+      for (int t = pair; t < P.total_tiles && ok; t += npairs, ++local) {
         const TileInfo ti = decode_tile(P, t);
         const DevProblem& pr = P.prob[ti.p];
         const int kblocks = (pr.k + BK - 1) / BK;
@@ -311,28 +365,30 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint64_t ad = make_sdesc_sw128(a_base + kk * 32, 16, 1024);
             const uint64_t bd = make_sdesc_sw128(b_base + kk * 32, 16, 1024);
-            umma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            umma2(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
-          umma_commit(&empty[stage]);
+          commit_both(&empty[stage]);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        umma_commit(&acc_full[acc]);
+        commit_both(&acc_full[acc]);
       }
-      // Every MMA this thread issued must be complete before TMEM is released.
-      umma_commit(drain);
+      asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(drain))
+                   : "memory");
       const uint64_t t0 = global_timer_ns();
       while (!mbar_try(drain, 0) && global_timer_ns() - t0 < 1000000000ull) {
       }
     }
   } else {
-    // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int q = warp & 3;
+    const uint32_t acc_empty_leader0 = map_to_rank(smem_u32(&acc_empty[0]), 0);
+    const uint32_t acc_empty_leader1 = map_to_rank(smem_u32(&acc_empty[1]), 0);
     int local = 0;
-    for (int t = blockIdx.x; t < P.total_tiles; t += gridDim.x, ++local) {
+    for (int t = pair; t < P.total_tiles; t += npairs, ++local) {
       const int acc = local & 1;
       bool ok = mbar_wait(&acc_full[acc], (uint32_t)(local >> 1) & 1u, wc, kSiteAccFull);
       ok = __all_sync(0xffffffffu, ok);
@@ -341,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       const TileInfo ti = decode_tile(P, t);
       const DevProblem& pr = P.prob[ti.p];
       const uint32_t tbase = tmem + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
-      const int r = ti.m_tile * BM + q * 32 + lane;
+      const int r = ti.m_tile * PAIR_M + (int)rank * BM + q * 32 + lane;
       const bool row_ok = r < pr.rows;
       const int col0 = ti.n_tile * BN;
       if (pr.epi == kEpiStore || pr.epi == kEpiResidual) {
@@ -363,9 +419,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 #pragma unroll
                 for (int i = 0; i < 32; ++i) o[i] = xr[i] + gsc * __uint_as_float(v[i]);
               } else {
+                float gv[32];
+                load_row32(grow + c * 32, gv);  // 16-byte loads of the gate vector
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                  o[i] = xr[i] + __bfloat162float(grow[c * 32 + i]) * __uint_as_float(v[i]);
+                for (int i = 0; i < 32; ++i) o[i] = xr[i] + gv[i] * __uint_as_float(v[i]);
               }
             } else {
 #pragma unroll
@@ -397,15 +454,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[acc]);
+      if (lane == 0) arrive_cluster(acc ? acc_empty_leader1 : acc_empty_leader0);
     }
   }
 
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();  // no MMA, TMA or remote arrive of the pair is still in flight
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
   }
 }
 
@@ -449,13 +506,13 @@ cudaError_t launch_gemm(const GemmProblemHost* probs, int nprob, int batch, floa
     if (!encode_tmap_bf16(&P.a_map[i], h.a, 3, adims, astr, abox)) return cudaErrorInvalidValue;
     const uint64_t bdims[2] = {(uint64_t)h.k, (uint64_t)h.n};
     const uint64_t bstr[1] = {(uint64_t)h.k * 2};
-    const uint32_t bbox[2] = {BK, BN};
+    const uint32_t bbox[2] = {BK, BN / 2};
     if (!encode_tmap_bf16(&P.b_map[i], h.w, 2, bdims, bstr, bbox)) return cudaErrorInvalidValue;
     d.rows = h.rows;
     d.a_row0 = h.a_row0;
     d.n = h.n;
     d.k = h.k;
-    d.m_tiles = (h.rows + BM - 1) / BM;
+    d.m_tiles = (h.rows + PAIR_M - 1) / PAIR_M;
     d.n_tiles = (h.n + BN - 1) / BN;
     d.tile_begin = tiles;
     d.epi = h.epi;
@@ -497,10 +554,10 @@ cudaError_t launch_gemm(const GemmProblemHost* probs, int nprob, int batch, floa
     if (e != cudaSuccess) return e;
     g_attr_set[dev] = true;
   }
-  const int sms = sm_count();
-  const int grid = tiles < sms ? tiles : sms;
+  const int pairs_max = sm_count() / 2;
+  const int pairs = tiles < pairs_max ? tiles : pairs_max;
   LaunchScope scope(cls, s);
-  gemm_kernel<<<grid, kThreads, kSmemBytes, s>>>(P);
+  gemm_kernel<<<2 * pairs, kThreads, kSmemBytes, s>>>(P);
   return cudaGetLastError();
 }
 
