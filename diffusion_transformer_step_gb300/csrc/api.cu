@@ -744,6 +744,12 @@ dit_status dit_sync_status(void* ws, dit_stream_t stream, uint32_t* where_out) {
   return DIT_OK;
 }
 
+dit_status dit_selftest_wait_timeout(void* ws, size_t ws_bytes, unsigned int limit_us, dit_stream_t stream) {
+  if (!aligned16(ws) || ws_bytes < sizeof(DeviceStatus) || limit_us < 1 || limit_us > 1000000)
+    return DIT_ERR_INVALID_ARG;
+  return cuda_status(launch_selftest_wait(status_of(ws), 1000ull * limit_us, (cudaStream_t)stream));
+}
+
 dit_status dit_adaln(int batch, int rows, int hidden, const void* x_dev, int x_rows, int x_row0, int split,
                      const void* shift_lo, const void* scale_lo, const void* shift_hi, const void* scale_hi,
                      long long mod_stride, float eps, void* y_dev, dit_stream_t stream) {

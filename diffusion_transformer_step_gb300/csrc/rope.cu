@@ -42,7 +42,27 @@ __global__ void pack_mlp_in_kernel(const bf16* __restrict__ src, bf16* __restric
   for (int c = threadIdx.x; c < cols / 8; c += blockDim.x) d[c] = s[c];
 }
 
+// Failure-detection self-test: one thread waits on an mbarrier that nothing arrives on,
+// with a short limit; the bounded wait gives up, records the timeout and its site in the
+// status word and the kernel returns normally.
+__global__ void selftest_wait_kernel(DeviceStatus* status, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  abort_flag = 0;
+  fence_mbar_init();
+  const WaitCtx wc{status, &abort_flag, limit_ns};
+  mbar_wait(&bar, 0, wc, kSelftestSite);
+}
+
 }  // namespace
+
+cudaError_t launch_selftest_wait(DeviceStatus* status, unsigned long long limit_ns, cudaStream_t s) {
+  LaunchScope scope(kClsRope, s);
+  selftest_wait_kernel<<<1, 32, 0, s>>>(status, limit_ns);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_rope_table(const int32_t* ids, int n, const int* axes_dim, float theta, float* table,
                               cudaStream_t s) {

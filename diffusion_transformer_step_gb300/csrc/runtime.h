@@ -82,6 +82,9 @@ cudaError_t launch_timestep_in(const bf16* t_in, int H, int time_dim, const floa
 cudaError_t launch_denoise_setup(const float* sigmas_host, int steps, int batch, float* sigma, float* coef,
                                  cudaStream_t s);
 
+constexpr uint32_t kSelftestSite = 0x901;
+cudaError_t launch_selftest_wait(DeviceStatus* status, unsigned long long limit_ns, cudaStream_t s);
+
 cudaError_t launch_rope_table(const int32_t* ids, int n, const int* axes_dim, float theta, float* table,
                               cudaStream_t s);
 cudaError_t launch_pack_mlp_in(const bf16* src, bf16* dst, int F, int cols, cudaStream_t s);

@@ -86,6 +86,7 @@ _SIGS = {
                                    _I, _P, C.POINTER(_P)]),
     "dit_graph_launch": (_I, [_P, _P]),
     "dit_graph_destroy": (_I, [_P]),
+    "dit_selftest_wait_timeout": (_I, [_P, _SZ, C.c_uint, _P]),
     "dit_launch_count": (C.c_ulonglong, []),
     "dit_timing_begin": (_I, [_I]),
     "dit_timing_end": (_I, [C.POINTER(_I), C.POINTER(_I), C.POINTER(_F), _I]),
@@ -281,6 +282,11 @@ def dit_modulation_static(w: dit_weights, sigma_dev, batch: int, mod_dev, stream
     batch <= 8, hidden <= 4096), for callers that cannot allocate device memory."""
     _check("dit_modulation_static", lib().dit_modulation_static(C.byref(w), _ptr(sigma_dev), batch, _ptr(mod_dev),
                                                                  _stream(stream)))
+
+
+def dit_selftest_wait_timeout(ws, ws_bytes: int, limit_us: int, stream=None):
+    """Launch the bounded-wait self-test kernel (a wait that can never complete)."""
+    _check("dit_selftest_wait_timeout", lib().dit_selftest_wait_timeout(_ptr(ws), ws_bytes, limit_us, _stream(stream)))
 
 
 def dit_launch_count() -> int:

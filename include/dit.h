@@ -242,6 +242,13 @@ dit_status dit_graph_launch(dit_graph graph, dit_stream_t stream);
 /* Release the graph (NULL is accepted). */
 dit_status dit_graph_destroy(dit_graph graph);
 
+/* Failure-detection self-test: launches one kernel whose only thread waits on a device
+ * barrier that nothing arrives on, with a limit of limit_us microseconds (1 .. 1e6).  The
+ * bounded wait gives up, records DIT_ERR_TIMEOUT's bit and the site id 0x901 in the
+ * workspace status word, and the kernel returns: dit_sync_status then reports
+ * DIT_ERR_TIMEOUT and the context stays usable.  ws: any workspace of >= 256 bytes. */
+dit_status dit_selftest_wait_timeout(void* ws, size_t ws_bytes, unsigned int limit_us, dit_stream_t stream);
+
 /* ---- Component operations (the kernels a block is made of) ---------------------- */
 
 /* Adaptive LayerNorm on rows of x: for batch b and row r < rows,

@@ -274,3 +274,24 @@ def test_denoise_loop_matches_stepwise_klein_1024(dit):
     d = Hx.cosine(Hx.to_np(x) - Hx.to_np(inp["img_tokens"]), Hx.to_np(want) - Hx.to_np(inp["img_tokens"]))
     print(f"denoise step_1024 vs stepwise: displacement-cos {d:.6f}")
     assert d >= 0.999
+
+
+# Three references of different aspect ratios (1024x1024, 768 high x 1344 wide, 1344 high x
+# 768 wide; t = 10, 20, 30) with a 1920x1088 target: the pages allow 1-3 references at
+# their own aspect ratio ("flux2-klein-p100a" task table).  N = 512 + 8160 + 12160 = 20832.
+REF3 = synth.Workload("ref3_1920x1088", synth.KLEIN, 1, 512, (68, 120), ((64, 64), (48, 84), (84, 48)))
+
+
+def test_dual_block_three_references_1920x1088(dit):
+    run_block(dit, "dual", REF3, seed=3)
+
+
+# A wider configuration through the same config-driven path (hidden 4096, 32 heads, MLP
+# 12288); the pages name a 9B variant without its widths, so these stand in for it.
+WIDE = synth.Widths(hidden=4096, heads=32, head_dim=128, mlp_hidden=12288, n_dual=1, n_single=1)
+WIDE_WL = synth.Workload("wide_4096", WIDE, 2, 64, (12, 20), ((4, 5),))
+
+
+@pytest.mark.parametrize("kind", ["dual", "single"])
+def test_blocks_wider_config(dit, kind):
+    run_block(dit, kind, WIDE_WL, seed=4)

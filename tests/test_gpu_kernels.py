@@ -161,3 +161,17 @@ def test_attention(dit, batch, heads, n, qscale, ws):
     want = O.attention(t(q), t(k), t(v)).reshape(batch, n, heads * 128)
     _cmp(out[..., :heads * 128], want, atol=3e-2, cos_min=0.999)
     assert (out[..., heads * 128:] == 0).all()
+
+
+def test_bounded_wait_reports_timeout_and_context_survives(dit, ws):
+    """A device wait that can never complete gives up after its limit: the status word
+    reports DIT_ERR_TIMEOUT with the waiting site, and later work on the GPU still runs."""
+    import time
+    t0 = time.perf_counter()
+    dit.dit_selftest_wait_timeout(ws, ws.numel(), 20000)
+    st, where = dit.dit_sync_status(ws)
+    assert st == dit.DIT_ERR_TIMEOUT and where == 0x901
+    assert time.perf_counter() - t0 < 5.0
+    st, _ = dit.dit_sync_status(ws)          # cleared by the previous read
+    assert st == dit.DIT_OK
+    test_attention(dit, 1, 1, 128, 1.0, ws)   # the context is still usable
