@@ -4,6 +4,8 @@
 // intermediate residual stream.  One warp per row: 128-bit loads, the row kept in registers, a
 // two-pass mean / variance with warp-shuffle reductions.  HBM-bound: each row is read
 // once (2H bytes) and written once (2H bytes); the modulation vectors stay in L1/L2.
+#include <cuda_fp8.h>
+
 #include "runtime.h"
 
 namespace dit {
@@ -12,7 +14,9 @@ namespace {
 
 constexpr int kRowsPerBlock = 8;  // 8 warps
 
-template <int VPL, bool F32IN>  // 8-element vectors per lane: hidden = VPL * 256
+// kFp8Out: y is written as e4m3 with one fp32 scale per row (y ~ scale * q, scale =
+// max|y| / 448, the largest finite e4m3), the A operand of an fp8 projection.
+template <int VPL, bool F32IN, bool kFp8Out>  // 8-element vectors per lane: hidden = VPL * 256
 __global__ void __launch_bounds__(kRowsPerBlock * 32) adaln_kernel(AdaLNArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long row = (long long)blockIdx.x * kRowsPerBlock + warp;
@@ -67,6 +71,7 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) adaln_kernel(AdaLNArgs a) 
   for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
   const float rstd = rsqrtf(sq * (1.0f / H) + a.eps);
 
+  float amax = 0.f;
 #pragma unroll
   for (int i = 0; i < VPL; ++i) {
     const uint4 sh = __ldg(shv + i * 32 + lane);
@@ -80,10 +85,63 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) adaln_kernel(AdaLNArgs a) 
       const float2 c2 = unpack_bf16x2(scw[j]);
       const float y0 = (1.0f + c2.x) * ((v[i][2 * j] - mean) * rstd) + s2.x;
       const float y1 = (1.0f + c2.y) * ((v[i][2 * j + 1] - mean) * rstd) + s2.y;
-      o[j] = pack_bf16x2(y0, y1);
+      if (kFp8Out) {
+        v[i][2 * j] = y0;
+        v[i][2 * j + 1] = y1;
+        amax = fmaxf(amax, fmaxf(fabsf(y0), fabsf(y1)));
+      } else {
+        o[j] = pack_bf16x2(y0, y1);
+      }
     }
-    yv[i * 32 + lane] = make_uint4(o[0], o[1], o[2], o[3]);
+    if (!kFp8Out) yv[i * 32 + lane] = make_uint4(o[0], o[1], o[2], o[3]);
   }
+  if (kFp8Out) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float scale = amax > 0.f ? amax / 448.0f : 1.0f;
+    const float inv = 1.0f / scale;
+    uint2* qv = reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(a.y_q) + b * a.y_bstride + (long long)r * H);
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      uint32_t w[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const __nv_fp8x2_storage_t lo =
+            __nv_cvt_float2_to_fp8x2(make_float2(v[i][4 * h] * inv, v[i][4 * h + 1] * inv), __NV_SATFINITE, __NV_E4M3);
+        const __nv_fp8x2_storage_t hi =
+            __nv_cvt_float2_to_fp8x2(make_float2(v[i][4 * h + 2] * inv, v[i][4 * h + 3] * inv), __NV_SATFINITE, __NV_E4M3);
+        w[h] = (uint32_t)lo | ((uint32_t)hi << 16);
+      }
+      qv[i * 32 + lane] = make_uint2(w[0], w[1]);
+    }
+    if (lane == 0) a.y_scale[(long long)b * a.rows + r] = scale;
+  }
+}
+
+// Per-row e4m3 quantisation of a weight: scale[r] = max|w[r, :]| / 448, q = w / scale.
+__global__ void quantize_rows_kernel(const bf16* __restrict__ w, int cols, uint8_t* __restrict__ q,
+                                     float* __restrict__ scale) {
+  const int r = blockIdx.x;
+  const bf16* wr = w + (long long)r * cols;
+  float amax = 0.f;
+  for (int c = threadIdx.x; c < cols; c += blockDim.x) amax = fmaxf(amax, fabsf(__bfloat162float(wr[c])));
+  __shared__ float red[32];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    amax = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if (threadIdx.x == 0) red[0] = amax;
+  }
+  __syncthreads();
+  const float s = red[0] > 0.f ? red[0] / 448.0f : 1.0f;
+  const float inv = 1.0f / s;
+  for (int c = threadIdx.x; c < cols; c += blockDim.x)
+    q[(long long)r * cols + c] = (uint8_t)__nv_cvt_float_to_fp8(__bfloat162float(wr[c]) * inv, __NV_SATFINITE, __NV_E4M3);
+  if (threadIdx.x == 0) scale[r] = s;
 }
 
 template <int VPL>
@@ -91,10 +149,12 @@ cudaError_t launch_vpl(const AdaLNArgs& a, cudaStream_t s) {
   const long long total = (long long)a.batch * a.rows;
   const unsigned grid = (unsigned)((total + kRowsPerBlock - 1) / kRowsPerBlock);
   LaunchScope scope(kClsAdaLN, s);
-  if (a.x_f32)
-    adaln_kernel<VPL, true><<<grid, kRowsPerBlock * 32, 0, s>>>(a);
+  if (a.y_q)
+    adaln_kernel<VPL, false, true><<<grid, kRowsPerBlock * 32, 0, s>>>(a);
+  else if (a.x_f32)
+    adaln_kernel<VPL, true, false><<<grid, kRowsPerBlock * 32, 0, s>>>(a);
   else
-    adaln_kernel<VPL, false><<<grid, kRowsPerBlock * 32, 0, s>>>(a);
+    adaln_kernel<VPL, false, false><<<grid, kRowsPerBlock * 32, 0, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -126,4 +186,13 @@ cudaError_t launch_adaln(const AdaLNArgs& a, cudaStream_t s) {
   }
 }
 
+}  // namespace dit
+
+namespace dit {
+cudaError_t launch_quantize_rows(const bf16* w, int rows, int cols, uint8_t* q, float* scale, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  LaunchScope scope(kClsPack, s);
+  quantize_rows_kernel<<<rows, 256, 0, s>>>(w, cols, q, scale);
+  return cudaGetLastError();
+}
 }  // namespace dit

@@ -61,8 +61,21 @@ int sm_count() {
   return n;
 }
 
+static bool encode_tmap_typed(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, int rank,
+                              const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box);
+
 bool encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
                       const uint64_t* strides_bytes, const uint32_t* box) {
+  return encode_tmap_typed(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, rank, dims, strides_bytes, box);
+}
+
+bool encode_tmap_u8(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                    const uint64_t* strides_bytes, const uint32_t* box) {
+  return encode_tmap_typed(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, rank, dims, strides_bytes, box);
+}
+
+static bool encode_tmap_typed(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, int rank,
+                              const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box) {
   typedef CUresult (*EncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -86,7 +99,7 @@ bool encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64
     es[i] = 1;
   }
   for (int i = 0; i + 1 < rank; ++i) st[i] = strides_bytes[i];
-  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), d, st, bx,
+  const CUresult r = fn(map, dtype, (cuuint32_t)rank, const_cast<void*>(base), d, st, bx,
                         es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -132,7 +145,7 @@ dit_status check_shape(const dit_shape* s) {
 inline size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Layout {
-  size_t status, h1, h2, mod, x, x1, y, q, k, v, cat;
+  size_t status, h1, h2, mod, x, x1, y, q, k, v, cat, yq, ascale;
   size_t in_img, in_ref, in_txt, in_sigma, out_vel;
   size_t den_sigma, den_coef, den_mod, den_h1, den_h2, den_state, den_xbf;
   size_t block_end, step_end, total;
@@ -156,6 +169,8 @@ Layout layout(const dit_config& c, const dit_shape& s) {
   L.v = take(B * N * H * 2);
   L.cat = take(B * N * (H + F) * 2);
   L.x1 = take(B * N * H * 4);
+  L.yq = take(B * N * H);
+  L.ascale = take(B * N * 4);
   L.block_end = o;
   L.mod = take(B * 17 * H * 2);
   L.x = take(B * N * H * 2);
@@ -304,12 +319,23 @@ dit_status run_single_block(const dit_weights* w, int layer, const dit_shape* s,
   const bf16* sh = mod + (long long)(kSingle + 0) * H;
   const bf16* sc = mod + (long long)(kSingle + 1) * H;
 
+  const dit_single_fp8* f8 = w->single_fp8 ? &w->single_fp8[layer] : nullptr;
   AdaLNArgs a1{B, N, H, x, 0, (long long)N * H, 0, y, (long long)N * H, 0, sh, sc, sh, sc, ms, c.eps};
+  if (f8) {
+    a1.y_q = at(ws, L.yq);
+    a1.y_scale = reinterpret_cast<float*>(at(ws, L.ascale));
+  }
   DIT_CUDA(launch_adaln(a1, st));
 
   GemmProblemHost p = blank_problem();
-  p.a = y; p.a_rows_total = N; p.lda = H; p.a_row0 = 0; p.rows = N;
-  p.w = (const bf16*)sw.qkv_mlp; p.n = 3 * H + 2 * F; p.k = H; p.epi = kEpiQKV;
+  p.a = f8 ? reinterpret_cast<const bf16*>(at(ws, L.yq)) : y;
+  p.a_rows_total = N; p.lda = H; p.a_row0 = 0; p.rows = N;
+  p.w = f8 ? (const bf16*)f8->qkv_mlp_q : (const bf16*)sw.qkv_mlp; p.n = 3 * H + 2 * F; p.k = H; p.epi = kEpiQKV;
+  if (f8) {
+    p.fp8 = 1;
+    p.a_scale = reinterpret_cast<const float*>(at(ws, L.ascale));
+    p.w_scale = f8->qkv_mlp_scale;
+  }
   p.n_qkv = 3 * H; p.hidden = H; p.q = q; p.kk = k; p.v = v;
   p.q_norm = (const bf16*)sw.q_norm; p.k_norm = (const bf16*)sw.k_norm; p.rope = rope; p.seq = N; p.tok0 = 0;
   p.out = cat; p.out_bstride = (long long)N * (H + F); p.ld_out = H + F; p.out_row0 = 0; p.out_col0 = H;
@@ -361,6 +387,8 @@ dit_status check_step_weights(const dit_weights* w) {
   for (int i = 0; i < w->cfg.n_single; ++i) {
     const dit_single_weights& s = w->single[i];
     if (!aligned16(s.qkv_mlp) || !aligned16(s.q_norm) || !aligned16(s.k_norm) || !aligned16(s.out))
+      return DIT_ERR_INVALID_ARG;
+    if (w->single_fp8 && (!aligned16(w->single_fp8[i].qkv_mlp_q) || !aligned16(w->single_fp8[i].qkv_mlp_scale)))
       return DIT_ERR_INVALID_ARG;
   }
   return DIT_OK;
@@ -536,6 +564,14 @@ dit_status dit_pack_mlp_in(const void* src_dev, void* dst_dev, int mlp_hidden, i
   return cuda_status(launch_pack_mlp_in((const bf16*)src_dev, (bf16*)dst_dev, mlp_hidden, cols, (cudaStream_t)stream));
 }
 
+dit_status dit_quantize_rows_fp8(const void* w_dev, int rows, int cols, void* q_dev, float* scale_dev,
+                                 dit_stream_t stream) {
+  if (!aligned16(w_dev) || !aligned16(q_dev) || !aligned16(scale_dev) || rows < 1 || cols < 16 || cols % 16 != 0)
+    return DIT_ERR_INVALID_ARG;
+  return cuda_status(launch_quantize_rows((const bf16*)w_dev, rows, cols, (uint8_t*)q_dev, scale_dev,
+                                          (cudaStream_t)stream));
+}
+
 dit_status dit_modulation(const dit_weights* w, const float* sigma_dev, int batch, void* mod_dev, void* ws,
                           size_t ws_bytes, dit_stream_t stream) {
   if (!w) return DIT_ERR_INVALID_ARG;
@@ -566,6 +602,8 @@ dit_status dit_single_block_fwd(const dit_weights* w, int layer, const dit_shape
   if (layer < 0 || layer >= w->cfg.n_single || !w->single) return DIT_ERR_INVALID_ARG;
   const dit_single_weights& s = w->single[layer];
   if (!aligned16(s.qkv_mlp) || !aligned16(s.q_norm) || !aligned16(s.k_norm) || !aligned16(s.out))
+    return DIT_ERR_INVALID_ARG;
+  if (w->single_fp8 && (!aligned16(w->single_fp8[layer].qkv_mlp_q) || !aligned16(w->single_fp8[layer].qkv_mlp_scale)))
     return DIT_ERR_INVALID_ARG;
   return run_single_block(w, layer, shape, (bf16*)x_dev, (const bf16*)mod_dev, rope_dev, ws, (cudaStream_t)stream);
 }

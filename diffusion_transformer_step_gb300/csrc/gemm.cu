@@ -57,6 +57,9 @@ struct DevProblem {
   const bf16* gate;
   long long gate_stride;
   const float* coef;
+  const float* a_scale;     // fp8 operands: per-row activation scales (row b*a_rows_total + a_row)
+  const float* w_scale;     // fp8 operands: per-output-column weight scales
+  int a_rows_total;
   int n_qkv, hidden;
   bf16 *q, *kk, *v;
   const bf16 *q_norm, *k_norm;
@@ -128,6 +131,33 @@ __device__ __forceinline__ void umma2(uint32_t d_tmem, uint64_t a_desc, uint64_t
   asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
                "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(acc) : "memory");
 }
+__device__ __forceinline__ void umma2_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t acc) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+               "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(acc) : "memory");
+}
+// Instruction descriptor of kind::f8f6f4 with e4m3 A and B (format code 0) and fp32 D.
+__host__ __device__ constexpr uint32_t make_idesc_e4m3(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Dequantised accumulator columns: acc * a_scale(row) * w_scale(col), in place.
+struct Dequant {
+  float as;          // this row's activation scale (1 when not quantised)
+  const float* ws;   // column scales of the tile (null when not quantised)
+};
+__device__ __forceinline__ void dequant32(uint32_t (&v)[32], const Dequant& dq, int col) {
+  if (!dq.ws) return;
+  const float4* w4 = reinterpret_cast<const float4*>(dq.ws + col);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float4 w = __ldg(w4 + i);
+    v[4 * i + 0] = __float_as_uint(__uint_as_float(v[4 * i + 0]) * dq.as * w.x);
+    v[4 * i + 1] = __float_as_uint(__uint_as_float(v[4 * i + 1]) * dq.as * w.y);
+    v[4 * i + 2] = __float_as_uint(__uint_as_float(v[4 * i + 2]) * dq.as * w.z);
+    v[4 * i + 3] = __float_as_uint(__uint_as_float(v[4 * i + 3]) * dq.as * w.w);
+  }
+}
+
 __device__ __forceinline__ void commit_both(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(smem_u32(bar)),
                "h"((uint16_t)3) : "memory");
@@ -175,12 +205,15 @@ __device__ __forceinline__ void load_row32_f32(const float* src, float* f) {
 }
 
 // SwiGLU over one packed 256-column accumulator: 128 outputs at dst[0..128).
-__device__ __forceinline__ void epi_swiglu(uint32_t tbase, bool row_ok, bf16* dst, int cols_left) {
+__device__ __forceinline__ void epi_swiglu(uint32_t tbase, bool row_ok, bf16* dst, int cols_left, const Dequant& dq,
+                                           int col0) {
 #pragma unroll 1
   for (int c = 0; c < 4; ++c) {
     uint32_t g[32], u[32];
     tmem_load32(tbase + c * 32, g);
     tmem_load32(tbase + 128 + c * 32, u);
+    dequant32(g, dq, col0 + c * 32);
+    dequant32(u, dq, col0 + 128 + c * 32);
     if (row_ok && c * 32 < cols_left) {
       float o[32];
 #pragma unroll
@@ -191,12 +224,13 @@ __device__ __forceinline__ void epi_swiglu(uint32_t tbase, bool row_ok, bf16* ds
 }
 
 __device__ __forceinline__ void epi_qkv_head(uint32_t tb, bool row_ok, int which, bf16* dst, const bf16* nw,
-                                             const float* rope_row, float eps) {
+                                             const float* rope_row, float eps, const Dequant& dq, int col0) {
   if (which == 2) {
 #pragma unroll 1
     for (int c = 0; c < 4; ++c) {
       uint32_t v[32];
       tmem_load32(tb + c * 32, v);
+      dequant32(v, dq, col0 + c * 32);
       if (row_ok) {
         float o[32];
 #pragma unroll
@@ -211,6 +245,7 @@ __device__ __forceinline__ void epi_qkv_head(uint32_t tb, bool row_ok, int which
   for (int c = 0; c < 4; ++c) {
     uint32_t v[32];
     tmem_load32(tb + c * 32, v);
+    dequant32(v, dq, col0 + c * 32);
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       const float x = __uint_as_float(v[i]);
@@ -222,6 +257,7 @@ __device__ __forceinline__ void epi_qkv_head(uint32_t tb, bool row_ok, int which
   for (int c = 0; c < 4; ++c) {
     uint32_t v[32];
     tmem_load32(tb + c * 32, v);
+    dequant32(v, dq, col0 + c * 32);
     if (row_ok) {
       float o[32];
       const float4* rp = reinterpret_cast<const float4*>(rope_row + c * 32);  // 16 pairs (cos, sin)
@@ -243,8 +279,12 @@ __device__ __forceinline__ void epi_qkv_head(uint32_t tb, bool row_ok, int which
   }
 }
 
+// kFp8: A and W are e4m3 (k-blocks of 128 elements, still 128-byte rows; kind::f8f6f4,
+// K 32 per MMA); the epilogue dequantises with the per-row and per-column scales.
+template <bool kFp8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ GemmParams P) {
+  constexpr int KB = kFp8 ? 128 : BK;  // elements per k-block
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -299,12 +339,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int t = pair; t < P.total_tiles && ok; t += npairs) {
         const TileInfo ti = decode_tile(P, t);
         const DevProblem& pr = P.prob[ti.p];
-        const int kblocks = (pr.k + BK - 1) / BK;
+        const int kblocks = (pr.k + KB - 1) / KB;
         const int arow = pr.a_row0 + ti.m_tile * PAIR_M + (int)rank * BM;
         const int brow = ti.n_tile * BN + (int)rank * (BN / 2);
         const bool pf = ti.m_tile == 0;
         for (int kb = 0; kb < kblocks; ++kb) {
-          if (pf && kb + 8 < kblocks) pf_l2(&P.b_map[ti.p], (kb + 8) * BK, brow);
+          if (pf && kb + 8 < kblocks) pf_l2(&P.b_map[ti.p], (kb + 8) * KB, brow);
           if (!mbar_wait(&empty[stage], phase ^ 1u, wc, kSiteEmpty)) {
             ok = false;
             break;
@@ -312,8 +352,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // both CTAs' loads complete on the leader's full barrier
           const uint32_t fb = map_to_rank(smem_u32(&full[stage]), 0);
           if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes);
-          tma3_2sm(sA + stage * kATileBytes, &P.a_map[ti.p], fb, kb * BK, arow, ti.b);
-          tma2_2sm(sB + stage * kBTileBytes, &P.b_map[ti.p], fb, kb * BK, brow);
+          tma3_2sm(sA + stage * kATileBytes, &P.a_map[ti.p], fb, kb * KB, arow, ti.b);
+          tma2_2sm(sB + stage * kBTileBytes, &P.b_map[ti.p], fb, kb * KB, brow);
           ++issued;
           if (++stage == kStages) {
             stage = 0;
@@ -338,14 +378,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (leader only)
     if (lane == 0 && rank == 0) {
-      const uint32_t idesc = make_idesc_bf16(PAIR_M, BN, false);
+      const uint32_t idesc = kFp8 ? make_idesc_e4m3(PAIR_M, BN) : make_idesc_bf16(PAIR_M, BN, false);
       uint32_t stage = 0, phase = 0;
       int local = 0;
       bool ok = true;
       for (int t = pair; t < P.total_tiles && ok; t += npairs, ++local) {
         const TileInfo ti = decode_tile(P, t);
         const DevProblem& pr = P.prob[ti.p];
-        const int kblocks = (pr.k + BK - 1) / BK;
+        const int kblocks = (pr.k + KB - 1) / KB;
         const int acc = local & 1;
         if (!mbar_wait(&acc_empty[acc], ((uint32_t)(local >> 1) & 1u) ^ 1u, wc, kSiteAccEmpty)) {
           ok = false;
@@ -362,10 +402,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint32_t a_base = smem_u32(sA + stage * kATileBytes);
           const uint32_t b_base = smem_u32(sB + stage * kBTileBytes);
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
+          for (int kk = 0; kk < 4; ++kk) {  // 32 bytes of K per MMA: 16 bf16 or 32 e4m3
             const uint64_t ad = make_sdesc_sw128(a_base + kk * 32, 16, 1024);
             const uint64_t bd = make_sdesc_sw128(b_base + kk * 32, 16, 1024);
-            umma2(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            if (kFp8)
+              umma2_f8(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            else
+              umma2(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
           commit_both(&empty[stage]);
           if (++stage == kStages) {
@@ -400,6 +443,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int r = ti.m_tile * PAIR_M + (int)rank * BM + q * 32 + lane;
       const bool row_ok = r < pr.rows;
       const int col0 = ti.n_tile * BN;
+      Dequant dq{1.0f, nullptr};
+      if (kFp8) {
+        dq.as = row_ok ? pr.a_scale[(long long)ti.b * pr.a_rows_total + pr.a_row0 + r] : 0.f;
+        dq.ws = pr.w_scale;
+      }
       if (pr.epi == kEpiStore || pr.epi == kEpiResidual) {
         const long long off = (long long)ti.b * pr.out_bstride + (long long)(pr.out_row0 + r) * pr.ld_out +
                               pr.out_col0 + col0;
@@ -409,6 +457,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t v[32];
           tmem_load32(tbase + c * 32, v);
+          if (kFp8 && col0 + c * 32 < pr.n) dequant32(v, dq, col0 + c * 32);
           if (row_ok && col0 + c * 32 < pr.n) {
             float o[32];
             if (pr.epi == kEpiResidual) {
@@ -437,7 +486,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int n_out = (pr.n - (pr.epi == kEpiQKV ? pr.n_qkv : 0)) / 2;
         bf16* orow = pr.out + (long long)ti.b * pr.out_bstride + (long long)(pr.out_row0 + r) * pr.ld_out +
                      pr.out_col0 + ocol;
-        epi_swiglu(tbase, row_ok, orow, n_out - ocol);
+        epi_swiglu(tbase, row_ok, orow, n_out - ocol, dq, col0);
       } else {
         const int which = col0 / pr.hidden;
         const int heads = pr.hidden / 128;
@@ -449,7 +498,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int hh = 0; hh < BN / 128; ++hh) {
           const int head = (col0 % pr.hidden) / 128 + hh;
           bf16* dst = base + (((long long)ti.b * heads + head) * pr.seq + tok) * 128;
-          epi_qkv_head(tbase + hh * 128, row_ok, which, dst, nw, rope_row, P.eps);
+          epi_qkv_head(tbase + hh * 128, row_ok, which, dst, nw, rope_row, P.eps, dq, col0 + hh * 128);
         }
       }
       tc_fence_before();
@@ -466,7 +515,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 }
 
-bool g_attr_set[16] = {false};
+bool g_attr_set[32] = {false};
 
 }  // namespace
 
@@ -500,14 +549,23 @@ cudaError_t launch_gemm(const GemmProblemHost* probs, int nprob, int batch, floa
       default:
         return cudaErrorInvalidValue;
     }
+    const int esz = h.fp8 ? 1 : 2;
+    if (h.fp8 != probs[0].fp8) return cudaErrorInvalidValue;
+    if (h.fp8 && (!h.a_scale || !h.w_scale || (h.k % 16) != 0)) return cudaErrorInvalidValue;
     const uint64_t adims[3] = {(uint64_t)h.k, (uint64_t)h.a_rows_total, (uint64_t)batch};
-    const uint64_t astr[2] = {(uint64_t)h.lda * 2, (uint64_t)h.lda * 2 * (uint64_t)h.a_rows_total};
-    const uint32_t abox[3] = {BK, BM, 1};
-    if (!encode_tmap_bf16(&P.a_map[i], h.a, 3, adims, astr, abox)) return cudaErrorInvalidValue;
+    const uint64_t astr[2] = {(uint64_t)h.lda * esz, (uint64_t)h.lda * esz * (uint64_t)h.a_rows_total};
+    const uint32_t kbx = h.fp8 ? 128 : BK;
+    const uint32_t abox[3] = {kbx, BM, 1};
     const uint64_t bdims[2] = {(uint64_t)h.k, (uint64_t)h.n};
-    const uint64_t bstr[1] = {(uint64_t)h.k * 2};
-    const uint32_t bbox[2] = {BK, BN / 2};
-    if (!encode_tmap_bf16(&P.b_map[i], h.w, 2, bdims, bstr, bbox)) return cudaErrorInvalidValue;
+    const uint64_t bstr[1] = {(uint64_t)h.k * esz};
+    const uint32_t bbox[2] = {kbx, BN / 2};
+    if (h.fp8) {
+      if (!encode_tmap_u8(&P.a_map[i], h.a, 3, adims, astr, abox)) return cudaErrorInvalidValue;
+      if (!encode_tmap_u8(&P.b_map[i], h.w, 2, bdims, bstr, bbox)) return cudaErrorInvalidValue;
+    } else {
+      if (!encode_tmap_bf16(&P.a_map[i], h.a, 3, adims, astr, abox)) return cudaErrorInvalidValue;
+      if (!encode_tmap_bf16(&P.b_map[i], h.w, 2, bdims, bstr, bbox)) return cudaErrorInvalidValue;
+    }
     d.rows = h.rows;
     d.a_row0 = h.a_row0;
     d.n = h.n;
@@ -528,6 +586,9 @@ cudaError_t launch_gemm(const GemmProblemHost* probs, int nprob, int batch, floa
     d.gate = h.gate;
     d.gate_stride = h.gate_stride;
     d.coef = h.coef;
+    d.a_scale = h.a_scale;
+    d.w_scale = h.w_scale;
+    d.a_rows_total = h.a_rows_total;
     d.n_qkv = h.n_qkv;
     d.hidden = h.hidden;
     d.q = h.q;
@@ -549,15 +610,23 @@ cudaError_t launch_gemm(const GemmProblemHost* probs, int nprob, int batch, floa
 
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 16 && !g_attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  const bool fp8 = probs[0].fp8 != 0;
+  const int slot = dev * 2 + (fp8 ? 1 : 0);
+  if (dev < 16 && !g_attr_set[slot]) {
+    cudaError_t e = fp8 ? cudaFuncSetAttribute(gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)kSmemBytes)
+                        : cudaFuncSetAttribute(gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    g_attr_set[dev] = true;
+    g_attr_set[slot] = true;
   }
   const int pairs_max = sm_count() / 2;
   const int pairs = tiles < pairs_max ? tiles : pairs_max;
   LaunchScope scope(cls, s);
-  gemm_kernel<<<2 * pairs, kThreads, kSmemBytes, s>>>(P);
+  if (fp8)
+    gemm_kernel<true><<<2 * pairs, kThreads, kSmemBytes, s>>>(P);
+  else
+    gemm_kernel<false><<<2 * pairs, kThreads, kSmemBytes, s>>>(P);
   return cudaGetLastError();
 }
 

@@ -49,6 +49,9 @@ int sm_count();
 // first; strides are in bytes for dims 1..rank-1.  Returns false on failure.
 bool encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
                       const uint64_t* strides_bytes, const uint32_t* box);
+// The same for a one-byte element type (e4m3 operands).
+bool encode_tmap_u8(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                    const uint64_t* strides_bytes, const uint32_t* box);
 
 // ---------------------------------------------------------------------------------
 // Launchers (each returns the launch's cudaError_t)
@@ -65,9 +68,15 @@ struct AdaLNArgs {
   const bf16 *shift_lo, *scale_lo, *shift_hi, *scale_hi;
   long long mod_stride;  // elements between batch rows of the modulation vectors
   float eps;
+  // Optional e4m3 output instead of y (bf16 x input only): y_q [batch, rows, hidden]
+  // bytes (batch stride y_bstride) and one fp32 scale per row, y_scale [batch, rows].
+  void* y_q;
+  float* y_scale;
 };
 bool adaln_supports(int hidden);  // hidden / 256 in {1..6, 8, 10, 12, 14, 16}
 cudaError_t launch_adaln(const AdaLNArgs& a, cudaStream_t s);
+// Per-row e4m3 quantisation of a bf16 weight [rows, cols]: q bytes, scale fp32 [rows].
+cudaError_t launch_quantize_rows(const bf16* w, int rows, int cols, uint8_t* q, float* scale, cudaStream_t s);
 
 // y[b, n] = act(sum_k W[n, k] x[b, k]); x fp32 [batch, k]; W bf16 [n, k].
 // act: 0 none, 1 SiLU.  Output fp32 (y_f32) or bf16 (y_bf16), exactly one non-null.
@@ -121,6 +130,12 @@ struct GemmProblemHost {
   const bf16* gate;
   long long gate_stride;
   const float* coef;
+  // e4m3 operands (fp8 != 0): A and W hold e4m3 bytes (lda in elements = bytes), the
+  // product is dequantised in the epilogue by a_scale[b * a_rows_total + a_row] and
+  // w_scale[col].  Every problem of one launch has the same fp8 setting.
+  int fp8;
+  const float* a_scale;
+  const float* w_scale;
   // QKV: columns [0, n_qkv) are q | k | v (each `hidden` wide); columns >= n_qkv are a
   // packed SwiGLU pair written to `out` at out_col0 + (col - n_qkv) / 2.
   int n_qkv, hidden;

@@ -50,10 +50,14 @@ class dit_single_weights(C.Structure):
     _fields_ = [(n, C.c_void_p) for n in ("qkv_mlp", "q_norm", "k_norm", "out")]
 
 
+class dit_single_fp8(C.Structure):
+    _fields_ = [("qkv_mlp_q", C.c_void_p), ("qkv_mlp_scale", C.c_void_p)]
+
+
 class dit_weights(C.Structure):
     _fields_ = [("cfg", dit_config), ("mod", dit_mod_weights), ("x_emb", C.c_void_p), ("ctx_emb", C.c_void_p),
                 ("proj_out", C.c_void_p), ("dual", C.POINTER(dit_dual_weights)),
-                ("single", C.POINTER(dit_single_weights))]
+                ("single", C.POINTER(dit_single_weights)), ("single_fp8", C.POINTER(dit_single_fp8))]
 
 
 _P = C.c_void_p
@@ -70,6 +74,7 @@ _SIGS = {
     "dit_token_ids": (_I, [C.POINTER(dit_shape), _I, _I, C.POINTER(_I), _I, _P]),
     "dit_rope_table": (_I, [C.POINTER(dit_config), _P, _I, _P, _P]),
     "dit_pack_mlp_in": (_I, [_P, _P, _I, _I, _P]),
+    "dit_quantize_rows_fp8": (_I, [_P, _I, _I, _P, _P, _P]),
     "dit_modulation": (_I, [C.POINTER(dit_weights), _P, _I, _P, _P, _SZ, _P]),
     "dit_dual_block_fwd": (_I, [C.POINTER(dit_weights), _I, C.POINTER(dit_shape), _P, _P, _P, _P, _SZ, _P]),
     "dit_single_block_fwd": (_I, [C.POINTER(dit_weights), _I, C.POINTER(dit_shape), _P, _P, _P, _P, _SZ, _P]),
@@ -186,6 +191,11 @@ def dit_rope_table(cfg: dit_config, ids_dev, n: int, table_dev, stream=None):
 
 def dit_pack_mlp_in(src_dev, dst_dev, mlp_hidden: int, cols: int, stream=None):
     _check("dit_pack_mlp_in", lib().dit_pack_mlp_in(_ptr(src_dev), _ptr(dst_dev), mlp_hidden, cols, _stream(stream)))
+
+
+def dit_quantize_rows_fp8(w_dev, rows: int, cols: int, q_dev, scale_dev, stream=None):
+    _check("dit_quantize_rows_fp8", lib().dit_quantize_rows_fp8(_ptr(w_dev), rows, cols, _ptr(q_dev), _ptr(scale_dev),
+                                                                 _stream(stream)))
 
 
 def dit_modulation(w: dit_weights, sigma_dev, batch: int, mod_dev, ws, ws_bytes: int, stream=None):
@@ -317,7 +327,7 @@ class DeviceWeights:
     ``synth.model_weights`` (logical layouts: MLP-in rows [gate; up]); MLP-in weights are
     rearranged on the device by dit_pack_mlp_in.  Keeps every tensor alive."""
 
-    def __init__(self, widths, logical: dict, device="cuda", n_dual=None, n_single=None):
+    def __init__(self, widths, logical: dict, device="cuda", n_dual=None, n_single=None, fp8=False):
         import torch
         self.widths = widths
         H, F = widths.hidden, widths.mlp_hidden
@@ -370,6 +380,18 @@ class DeviceWeights:
             s.out = dev(src["out"]).data_ptr()
         w.dual = C.cast(self._dual, C.POINTER(dit_dual_weights))
         w.single = C.cast(self._single, C.POINTER(dit_single_weights))
+        if fp8 and ns > 0:
+            # e4m3 copies of the fused single-stream projections (packed row order)
+            self._single_fp8 = (dit_single_fp8 * ns)()
+            rows = 3 * H + 2 * F
+            for i in range(ns):
+                q = torch.empty((rows, H), dtype=torch.uint8, device=device)
+                sc = torch.empty((rows,), dtype=torch.float32, device=device)
+                dit_quantize_rows_fp8(self._single[i].qkv_mlp, rows, H, q, sc)
+                keep += [q, sc]
+                self._single_fp8[i].qkv_mlp_q = q.data_ptr()
+                self._single_fp8[i].qkv_mlp_scale = sc.data_ptr()
+            w.single_fp8 = C.cast(self._single_fp8, C.POINTER(dit_single_fp8))
         self.w = w
         self._keep = keep
         torch.cuda.synchronize()

@@ -99,15 +99,31 @@ typedef struct {
   const void *qkv_mlp, *q_norm, *k_norm, *out;
 } dit_single_weights;
 
+/* Low-precision copy of a single-stream block's fused projection (the "dit_prec" precision
+ * knob of the "tt_flux2_klein -- Python reference" KleinTT constructor): qkv_mlp_q
+ * [3H + 2F, H] e4m3 bytes in the same (packed) row order as qkv_mlp, and qkv_mlp_scale
+ * [3H + 2F] fp32, one per output row, with qkv_mlp ~= scale[n] * q[n, :] (from
+ * dit_quantize_rows_fp8). */
+typedef struct {
+  const void* qkv_mlp_q;
+  const float* qkv_mlp_scale;
+} dit_single_fp8;
+
 /* All weights.  `dual` and `single` are HOST arrays of n_dual and n_single entries
  * (they hold device pointers); they must stay valid for the duration of each call.
- * x_emb [H, in_channels], ctx_emb [H, txt_dim], proj_out [in_channels, H]. */
+ * x_emb [H, in_channels], ctx_emb [H, txt_dim], proj_out [in_channels, H].
+ * single_fp8: NULL for the bf16 path; else a HOST array of n_single entries, and every
+ * single-stream block runs its fused QKV + MLP-in projection in e4m3 (the modulated
+ * activations are quantised per token row by the adaLN kernel, the product is
+ * dequantised in the GEMM epilogue before RMSNorm / RoPE / SwiGLU); everything else
+ * stays bf16. */
 typedef struct {
   dit_config cfg;
   dit_mod_weights mod;
   const void *x_emb, *ctx_emb, *proj_out;
   const dit_dual_weights* dual;
   const dit_single_weights* single;
+  const dit_single_fp8* single_fp8;
 } dit_weights;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -149,6 +165,12 @@ dit_status dit_rope_table(const dit_config* cfg, const int32_t* ids_dev, int n, 
  * weight, pack its last 2F rows (pointer offset 3H * cols elements) and copy the first
  * 3H rows unchanged. */
 dit_status dit_pack_mlp_in(const void* src_dev, void* dst_dev, int mlp_hidden, int cols, dit_stream_t stream);
+
+/* Weight preparation for the e4m3 path: for each row r of w_dev [rows, cols] (bf16),
+ * scale_dev[r] = max|w[r, :]| / 448 and q_dev[r, c] = e4m3(w[r, c] / scale[r]) (round to
+ * nearest, saturating).  q_dev [rows, cols] bytes, scale_dev [rows] fp32; cols % 16 == 0. */
+dit_status dit_quantize_rows_fp8(const void* w_dev, int rows, int cols, void* q_dev, float* scale_dev,
+                                 dit_stream_t stream);
 
 /* Global modulation of one step ("flux2-klein-p100a" Caveats: computed once per step and
  * shared by all blocks).  tau = 1000 * sigma; s = [cos(tau f_k) | sin(tau f_k)],
