@@ -14,9 +14,19 @@
 //               S row streamed from TMEM in 32-key chunks, exp2 against the running
 //               maximum with log2(e)/sqrt(d) folded in, P rounded to bf16 and written back
 //               into TMEM over its own S, where the PV MMA reads it as its A operand.  The
-//               running maximum is lazy: it (and O, in TMEM) is updated only when a key
-//               exceeds it by more than 2^8, which keeps every P <= 256 and is exact after
-//               the final 1/l; only then (and on the first key block) is S read twice.
+//               running maximum is lazy: the exponentials of a key block are taken against
+//               the maximum so far, and only when the block's row sum of P passes 2^12 (some
+//               key exceeded the maximum by more than 12 in log2 units) are the block
+//               maximum, the rescale of O (in TMEM) and the exponentials redone; the result is
+//               exact after the final 1/l.  Only then (and on the first key block) is S read
+//               twice, and the common path computes no maximum at all.
+// Why the common path avoids 3-input max and scalar FP32 arithmetic: on sm_103a a warp that
+// issues tcgen05.mma competes for issue slots with the other warps of its SM sub-partition,
+// and dense scalar FMA / max / byte-permute streams there slow the MMA issue several-fold
+// (measured: 64 -> 88 cycles per M128 N128 K16 MMA under dense 3-input max, -> 340 under
+// dense scalar FMA), while packed fp32x2 FMA/add, MUFU ex2 and bf16x2 conversion do not.
+// The MMA thread issues from descriptors computed once, and waiting warps sleep on the
+// barrier instead of spinning, for the same reason.
 // Ordering: MMAs issued by one thread execute in order and a commit tracks every earlier
 // MMA of that thread, so "S_t of block j+1 is ready" also means "P_t V_j is complete":
 // the softmax may then rescale O_t and overwrite P_t without a further wait.
@@ -40,7 +50,7 @@ constexpr uint32_t kOffV = kOffK + 2 * kTileBytes;
 constexpr uint32_t kOffBar = kOffV + 2 * kTileBytes;
 constexpr size_t kSmemBytes = 1024 + kOffBar + 256;
 constexpr uint32_t kTmemCols = 512;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr float kPsumLimit = 4096.0f;  // row sum of P that sends a key block down the slow path
 
 struct alignas(64) AttnParams {
   CUtensorMap q_map, k_map, v_map;
@@ -77,11 +87,11 @@ __device__ __forceinline__ void fadd2(float& s0, float& s1, float a0, float a1) 
   asm("mov.b64 {%0, %1}, %2;" : "=f"(s0), "=f"(s1) : "l"(S));
 }
 
-// One 32-key chunk of a softmax row: running key maximum (raw scores), P = 2^(s c - m)
-// packed to bf16 pairs, and the two partial row sums; kTail: keys at or past kv_valid
-// masked to -inf.  Every exponential runs on MUFU: moving a share of them to an FMA-pipe
-// polynomial was measured slower here (the softmax is latency-, not MUFU-bound).
-template <bool kTail>
+// One 32-key chunk of a softmax row: P = 2^(s c - m) packed to bf16 pairs and the two
+// partial row sums; kMax: also the running key maximum (raw scores); kTail: keys at or past
+// kv_valid masked to -inf.  Every exponential runs on MUFU: moving a share of them to an
+// FMA-pipe polynomial was measured slower here.
+template <bool kTail, bool kMax>
 __device__ __forceinline__ void softmax_chunk(const uint32_t (&r)[32], int base, int kv_valid, float c, float mneg,
                                               float& smax, float& ps0, float& ps1, uint32_t* pk) {
 #pragma unroll
@@ -91,7 +101,7 @@ __device__ __forceinline__ void softmax_chunk(const uint32_t (&r)[32], int base,
       if (base + i >= kv_valid) s0 = -INFINITY;
       if (base + i + 1 >= kv_valid) s1 = -INFINITY;
     }
-    smax = fmax3(smax, s0, s1);
+    if (kMax) smax = fmax3(smax, s0, s1);
     float x0, x1;
     ffma2(x0, x1, s0, s1, c, mneg);
     const float p0 = ex2_approx(x0);
@@ -101,7 +111,7 @@ __device__ __forceinline__ void softmax_chunk(const uint32_t (&r)[32], int base,
   }
 }
 
-template <bool kTail>
+template <bool kTail, bool kMax>
 __device__ __forceinline__ void softmax_row(uint32_t tS, int kv_valid, float c, float mneg, float& smax, float& psum,
                                             uint32_t (&pk)[64]) {
   float ps0 = 0.f, ps1 = 0.f;
@@ -109,7 +119,7 @@ __device__ __forceinline__ void softmax_row(uint32_t tS, int kv_valid, float c, 
   for (int q = 0; q < 4; ++q) {
     uint32_t r[32];
     tmem_load32(tS + q * 32, r);
-    softmax_chunk<kTail>(r, q * 32, kv_valid, c, mneg, smax, ps0, ps1, &pk[q * 16]);
+    softmax_chunk<kTail, kMax>(r, q * 32, kv_valid, c, mneg, smax, ps0, ps1, &pk[q * 16]);
   }
   psum = ps0 + ps1;
 }
@@ -119,28 +129,69 @@ enum : uint32_t {
 };
 
 
-__device__ __forceinline__ void issue_qk(uint8_t* smem, uint32_t tmem, int t, int st, uint32_t idesc, uint64_t* bar) {
-  const uint32_t sQ = smem_u32(smem + kOffQ + t * kTileBytes);
-  const uint32_t sK = smem_u32(smem + kOffK + st * kTileBytes);
+// Shared-memory descriptors of every MMA operand, computed once: Q_t (A of S_t = Q_t K^T),
+// K and V of both ring stages (B operands), per 16-wide K step.
+struct Descs {
+  uint64_t q[2][8], k[2][8], v[2][8];
+};
+
+__device__ __forceinline__ void make_descs(uint8_t* smem, Descs& d) {
+#pragma unroll
+  for (int t = 0; t < 2; ++t)
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+      d.q[t][kk] = make_sdesc_sw128(smem_u32(smem + kOffQ + t * kTileBytes) + off, 16, 1024);
+      d.k[t][kk] = make_sdesc_sw128(smem_u32(smem + kOffK + t * kTileBytes) + off, 16, 1024);
+      d.v[t][kk] = make_sdesc_sw128(smem_u32(smem + kOffV + t * kTileBytes) + kk * 2048, kHalfBytes, 1024);
+    }
+}
+
+// S_t = Q_t K^T (K from ring stage ST), then arrive on `bar` when done.
+template <int ST>
+__device__ __forceinline__ void issue_qk(const Descs& d, uint32_t tmem, int t, uint32_t idesc, uint64_t* bar) {
   const uint32_t tS = tmem + (uint32_t)(t * 256);
 #pragma unroll
-  for (int kk = 0; kk < 8; ++kk) {
-    const uint64_t ad = make_sdesc_sw128(sQ + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
-    const uint64_t bd = make_sdesc_sw128(sK + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
-    umma_bf16(tS, ad, bd, idesc, kk > 0 ? 1u : 0u);
-  }
+  for (int kk = 0; kk < 8; ++kk) umma_bf16(tS, d.q[t][kk], d.k[ST][kk], idesc, kk > 0 ? 1u : 0u);
   umma_commit(bar);
 }
 
-__device__ __forceinline__ void issue_pv(uint8_t* smem, uint32_t tmem, int t, int st, bool acc, uint32_t idesc) {
-  const uint32_t sV = smem_u32(smem + kOffV + st * kTileBytes);
+// O_t (+)= P_t V (V from ring stage ST), P_t read from TMEM over S_t.
+template <int ST>
+__device__ __forceinline__ void issue_pv(const Descs& d, uint32_t tmem, int t, bool acc, uint32_t idesc) {
   const uint32_t tP = tmem + (uint32_t)(t * 256);
   const uint32_t tO = tmem + (uint32_t)(t * 256 + 128);
 #pragma unroll
-  for (int kk = 0; kk < 8; ++kk) {
-    const uint64_t bd = make_sdesc_sw128(sV + kk * 2048, kHalfBytes, 1024);
-    umma_bf16_ts(tO, tP + kk * 8, bd, idesc, (acc || kk > 0) ? 1u : 0u);
+  for (int kk = 0; kk < 8; ++kk) umma_bf16_ts(tO, tP + kk * 8, d.v[ST][kk], idesc, (acc || kk > 0) ? 1u : 0u);
+}
+
+// One key block j (ring stage ST = j & 1) of the MMA issuer:
+//   O0 += P0 V_j, S0 = Q0 K_{j+1}^T, O1 += P1 V_j, S1 = Q1 K_{j+1}^T.
+template <int ST>
+__device__ __forceinline__ bool mma_block(const Descs& d, uint32_t tmem, int j, int nkv, uint32_t idesc_qk,
+                                          uint32_t idesc_pv, uint64_t* k_full, uint64_t* k_empty, uint64_t* v_full,
+                                          uint64_t* v_empty, uint64_t* s_full, uint64_t* p_full, const WaitCtx& wc) {
+  constexpr int NST = ST ^ 1;
+  const bool more = j + 1 < nkv;
+  if (!mbar_wait(&v_full[ST], (uint32_t)(j >> 1) & 1u, wc, kSiteVFull) ||
+      !mbar_wait(&p_full[0], (uint32_t)j & 1u, wc, kSitePFull))
+    return false;
+  tc_fence_after();
+  issue_pv<ST>(d, tmem, 0, j > 0, idesc_pv);
+  if (more) {
+    if (!mbar_wait(&k_full[NST], (uint32_t)((j + 1) >> 1) & 1u, wc, kSiteKFull)) return false;
+    tc_fence_after();
+    issue_qk<NST>(d, tmem, 0, idesc_qk, &s_full[0]);
   }
+  if (!mbar_wait(&p_full[1], (uint32_t)j & 1u, wc, kSitePFull)) return false;
+  tc_fence_after();
+  issue_pv<ST>(d, tmem, 1, j > 0, idesc_pv);
+  umma_commit(&v_empty[ST]);
+  if (more) {
+    issue_qk<NST>(d, tmem, 1, idesc_qk, &s_full[1]);
+    umma_commit(&k_empty[NST]);
+  }
+  return true;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_constant__ AttnParams P) {
@@ -244,42 +295,20 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
     if (lane == 0) {
       const uint32_t idesc_qk = make_idesc_bf16(128, 128, false);
       const uint32_t idesc_pv = make_idesc_bf16(128, 128, true);
+      Descs d;
+      make_descs(smem, d);
       bool ok = mbar_wait(q_full, 0, wc, kSiteQ) && mbar_wait(&k_full[0], 0, wc, kSiteKFull);
       if (ok) {
         tc_fence_after();
-        issue_qk(smem, tmem, 0, 0, idesc_qk, &s_full[0]);
-        issue_qk(smem, tmem, 1, 0, idesc_qk, &s_full[1]);
+        issue_qk<0>(d, tmem, 0, idesc_qk, &s_full[0]);
+        issue_qk<0>(d, tmem, 1, idesc_qk, &s_full[1]);
         umma_commit(&k_empty[0]);
       }
-      for (int j = 0; j < nkv && ok; ++j) {
-        const int st = j & 1, nst = (j + 1) & 1;
-        const bool more = j + 1 < nkv;
-        if (!mbar_wait(&v_full[st], (uint32_t)(j >> 1) & 1u, wc, kSiteVFull) ||
-            !mbar_wait(&p_full[0], (uint32_t)j & 1u, wc, kSitePFull)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        issue_pv(smem, tmem, 0, st, j > 0, idesc_pv);
-        if (more) {
-          if (!mbar_wait(&k_full[nst], (uint32_t)((j + 1) >> 1) & 1u, wc, kSiteKFull)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          issue_qk(smem, tmem, 0, nst, idesc_qk, &s_full[0]);
-        }
-        if (!mbar_wait(&p_full[1], (uint32_t)j & 1u, wc, kSitePFull)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        issue_pv(smem, tmem, 1, st, j > 0, idesc_pv);
-        umma_commit(&v_empty[st]);
-        if (more) {
-          issue_qk(smem, tmem, 1, nst, idesc_qk, &s_full[1]);
-          umma_commit(&k_empty[nst]);
-        }
+      for (int j = 0; j < nkv && ok; j += 2) {
+        ok = mma_block<0>(d, tmem, j, nkv, idesc_qk, idesc_pv, k_full, k_empty, v_full, v_empty, s_full, p_full, wc);
+        if (ok && j + 1 < nkv)
+          ok = mma_block<1>(d, tmem, j + 1, nkv, idesc_qk, idesc_pv, k_full, k_empty, v_full, v_empty, s_full, p_full,
+                            wc);
       }
       umma_commit(o_done);
       umma_commit(drain);
@@ -299,23 +328,24 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
-      ok = mbar_wait(&s_full[tile], (uint32_t)j & 1u, wc, kSiteSFull);
+      ok = mbar_wait_sleep(&s_full[tile], (uint32_t)j & 1u, wc, kSiteSFull);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
       const int kv_valid = n - j * kBKV;
       // Fast path: exponentials against the running maximum, streamed over four
-      // 32-key chunks of S, only the packed P kept.  Valid unless some key exceeds the
-      // running maximum by more than 2^8 (and always wrong on the first key block).
+      // 32-key chunks of S, only the packed P kept.  Valid while the row sum of P stays
+      // at or below kPsumLimit (no key far above the running maximum); never on the first
+      // key block, which has no maximum yet.  NaN scores keep the fast path.
       uint32_t pk[64];
       float psum = 0.f, smax = -INFINITY;
       bool slow = (j == 0);
       if (!slow) {
         if (kv_valid >= kBKV)
-          softmax_row<false>(tS, kv_valid, c, -m_run, smax, psum, pk);
+          softmax_row<false, false>(tS, kv_valid, c, -m_run, smax, psum, pk);
         else
-          softmax_row<true>(tS, kv_valid, c, -m_run, smax, psum, pk);
-        slow = smax * c > m_run + kRescaleThreshold;
+          softmax_row<true, false>(tS, kv_valid, c, -m_run, smax, psum, pk);
+        slow = psum > kPsumLimit;
       }
       float alpha = 1.0f;
       if (__any_sync(0xffffffffu, slow)) {
@@ -333,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
         bool resc = false;
         if (j == 0) {
           m_run = m_cand;
-        } else if (m_cand > m_run + kRescaleThreshold) {
+        } else if (m_cand > m_run) {
           alpha = ex2_approx(m_run - m_cand);
           m_run = m_cand;
           resc = true;
@@ -352,9 +382,9 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
         }
         float unused = -INFINITY;
         if (kv_valid >= kBKV)
-          softmax_row<false>(tS, kv_valid, c, -m_run, unused, psum, pk);
+          softmax_row<false, false>(tS, kv_valid, c, -m_run, unused, psum, pk);
         else
-          softmax_row<true>(tS, kv_valid, c, -m_run, unused, psum, pk);
+          softmax_row<true, false>(tS, kv_valid, c, -m_run, unused, psum, pk);
       }
       l_run = l_run * alpha + psum;
       // P_t over S_t columns [0, 64): keys [2c, 2c + 1] in column c
@@ -366,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
       if (lane == 0) mbar_arrive(&p_full[tile]);
     }
     if (ok) {
-      bool ok2 = mbar_wait(o_done, 0, wc, kSiteODone);
+      bool ok2 = mbar_wait_sleep(o_done, 0, wc, kSiteODone);
       ok2 = __all_sync(0xffffffffu, ok2);
       if (ok2) {
         tc_fence_after();

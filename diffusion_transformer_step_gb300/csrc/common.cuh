@@ -115,6 +115,44 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   return mbar_wait_slow(bar, parity, w, site);
 }
 
+// The same bounded wait for warps that have nothing else to do meanwhile: try_wait with a
+// suspend-time hint lets the thread sleep in hardware until the phase completes (or the hint
+// elapses) instead of spinning on issue slots that a computing or MMA-issuing warp of the
+// same SM sub-partition needs.  The limit and abort checks run after every return.
+constexpr uint32_t kSleepHintNs = 1000000u;  // 1 ms
+
+__device__ __forceinline__ bool mbar_try_sleep(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kSleepHintNs)
+      : "memory");
+  return ok != 0;
+}
+
+static __device__ __noinline__ bool mbar_wait_sleep_slow(uint64_t* bar, uint32_t parity, const WaitCtx& w,
+                                                         uint32_t site) {
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    if (mbar_try_sleep(bar, parity)) return true;
+    if (*w.abort_flag) return false;
+    if (global_timer_ns() - t0 > w.limit_ns) {
+      if (atomicOr(&w.status->word, kStatusTimeout) == 0u) atomicExch(&w.status->where, site);
+      *w.abort_flag = 1;
+      __threadfence_block();
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, const WaitCtx& w, uint32_t site) {
+  if (mbar_try_sleep(bar, parity)) return true;
+  return mbar_wait_sleep_slow(bar, parity, w, site);
+}
+
 // ---------------------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor) tile loads into shared memory, completing on an mbarrier.
 // ---------------------------------------------------------------------------------
