@@ -16,7 +16,12 @@
 //   warps 2-5   epilogue in both CTAs: one thread per accumulator row of its own CTA,
 //               tcgen05.ld 32 columns at a time, fused math, 16-byte global stores; the
 //               accumulator is handed back on the leader's barrier (8 arrivals).
-// The two accumulators let tile i's epilogue overlap tile i+1's main loop.  Up to two
+// The two accumulators let tile i's epilogue overlap tile i+1's main loop.  Because the
+// MMA-issuing warp competes for issue slots with the epilogue warp of its SM sub-partition
+// (on sm_103a dense scalar FP32 FMA there slows tcgen05.mma issue several-fold, packed
+// fp32x2 arithmetic does not), the epilogue maths runs on packed fp32x2 FMA / multiply / add
+// with MUFU exponentials and reciprocals, the issuer advances precomputed descriptors with
+// one add per MMA, and waiting warps sleep on their barriers.  Up to two
 // problems (the text and image streams of a dual-stream block) share one launch; tiles
 // are ordered with M fastest so that concurrent pairs share the same weight slab in L2.
 //
@@ -127,6 +132,17 @@ __device__ __forceinline__ void pf_l2(const CUtensorMap* m, int x, int y) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(m)),
                "r"(x), "r"(y) : "memory");
 }
+// Advance a shared-memory descriptor by `units` x 16 bytes: the start-address field is
+// the low 14 bits, and no shared-memory address reaches 2^18 bytes, so the add never
+// carries out of the field.
+__device__ __forceinline__ uint64_t desc_advance(uint64_t d, uint32_t units) {
+  uint32_t lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(d));
+  lo += units;
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
 __device__ __forceinline__ void umma2(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t acc) {
   asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
                "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(acc) : "memory");
@@ -140,6 +156,17 @@ __host__ __device__ constexpr uint32_t make_idesc_e4m3(int M, int N) {
   return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// Packed fp32x2 arithmetic (one instruction for two lanes of a row).
+__device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
+__device__ __forceinline__ float2 acc2(const uint32_t (&v)[32], int i) {
+  return make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Dequantised accumulator columns: acc * a_scale(row) * w_scale(col), in place.
 struct Dequant {
   float as;          // this row's activation scale (1 when not quantised)
@@ -148,13 +175,16 @@ struct Dequant {
 __device__ __forceinline__ void dequant32(uint32_t (&v)[32], const Dequant& dq, int col) {
   if (!dq.ws) return;
   const float4* w4 = reinterpret_cast<const float4*>(dq.ws + col);
+  const float2 as2 = f2(dq.as, dq.as);
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const float4 w = __ldg(w4 + i);
-    v[4 * i + 0] = __float_as_uint(__uint_as_float(v[4 * i + 0]) * dq.as * w.x);
-    v[4 * i + 1] = __float_as_uint(__uint_as_float(v[4 * i + 1]) * dq.as * w.y);
-    v[4 * i + 2] = __float_as_uint(__uint_as_float(v[4 * i + 2]) * dq.as * w.z);
-    v[4 * i + 3] = __float_as_uint(__uint_as_float(v[4 * i + 3]) * dq.as * w.w);
+    const float2 a = __fmul2_rn(__fmul2_rn(acc2(v, 2 * i), as2), f2(w.x, w.y));
+    const float2 b = __fmul2_rn(__fmul2_rn(acc2(v, 2 * i + 1), as2), f2(w.z, w.w));
+    v[4 * i + 0] = __float_as_uint(a.x);
+    v[4 * i + 1] = __float_as_uint(a.y);
+    v[4 * i + 2] = __float_as_uint(b.x);
+    v[4 * i + 3] = __float_as_uint(b.y);
   }
 }
 
@@ -205,8 +235,10 @@ __device__ __forceinline__ void load_row32_f32(const float* src, float* f) {
 }
 
 // SwiGLU over one packed 256-column accumulator: 128 outputs at dst[0..128).
+// silu(g) = g / (1 + 2^(-g log2 e)) with MUFU ex2 and rcp.approx.
 __device__ __forceinline__ void epi_swiglu(uint32_t tbase, bool row_ok, bf16* dst, int cols_left, const Dequant& dq,
                                            int col0) {
+  const float2 nl2e = f2(-1.4426950408889634f, -1.4426950408889634f), one = f2(1.0f, 1.0f);
 #pragma unroll 1
   for (int c = 0; c < 4; ++c) {
     uint32_t g[32], u[32];
@@ -217,12 +249,21 @@ __device__ __forceinline__ void epi_swiglu(uint32_t tbase, bool row_ok, bf16* ds
     if (row_ok && c * 32 < cols_left) {
       float o[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) o[i] = silu_f(__uint_as_float(g[i])) * __uint_as_float(u[i]);
+      for (int i = 0; i < 16; ++i) {
+        const float2 gg = acc2(g, i);
+        float2 t = __fmul2_rn(gg, nl2e);
+        t = __fadd2_rn(f2(ex2_approx(t.x), ex2_approx(t.y)), one);
+        const float2 r = __fmul2_rn(__fmul2_rn(gg, f2(rcp_approx(t.x), rcp_approx(t.y))), acc2(u, i));
+        o[2 * i] = r.x;
+        o[2 * i + 1] = r.y;
+      }
       store_row32(dst + c * 32, o);
     }
   }
 }
 
+// One 128-column head of the QKV projection: V stored as is; Q and K get RMSNorm over the
+// head (fp32, eps) times the learned weight, then RoPE on adjacent pairs from the table.
 __device__ __forceinline__ void epi_qkv_head(uint32_t tb, bool row_ok, int which, bf16* dst, const bf16* nw,
                                              const float* rope_row, float eps, const Dequant& dq, int col0) {
   if (which == 2) {
@@ -240,25 +281,28 @@ __device__ __forceinline__ void epi_qkv_head(uint32_t tb, bool row_ok, int which
     }
     return;
   }
-  float ss = 0.f;
+  float2 ss2 = f2(0.f, 0.f);
 #pragma unroll 1
   for (int c = 0; c < 4; ++c) {
     uint32_t v[32];
     tmem_load32(tb + c * 32, v);
     dequant32(v, dq, col0 + c * 32);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const float x = __uint_as_float(v[i]);
-      ss += x * x;
+    for (int i = 0; i < 16; ++i) {
+      const float2 x = acc2(v, i);
+      ss2 = __ffma2_rn(x, x, ss2);
     }
   }
-  const float rs = rsqrtf(ss * (1.0f / 128.0f) + eps);
+  const float rs = rsqrtf((ss2.x + ss2.y) * (1.0f / 128.0f) + eps);
+  const float2 rs2 = f2(rs, rs);
 #pragma unroll 1
   for (int c = 0; c < 4; ++c) {
     uint32_t v[32];
     tmem_load32(tb + c * 32, v);
     dequant32(v, dq, col0 + c * 32);
     if (row_ok) {
+      float w[32];
+      load_row32(nw + c * 32, w);  // 16-byte loads of the norm weights
       float o[32];
       const float4* rp = reinterpret_cast<const float4*>(rope_row + c * 32);  // 16 pairs (cos, sin)
 #pragma unroll
@@ -267,11 +311,12 @@ __device__ __forceinline__ void epi_qkv_head(uint32_t tb, bool row_ok, int which
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int d = 2 * (p + h);
-          const float c0 = h ? cs.z : cs.x, s0 = h ? cs.w : cs.y;
-          const float x0 = __uint_as_float(v[d]) * rs * __bfloat162float(nw[c * 32 + d]);
-          const float x1 = __uint_as_float(v[d + 1]) * rs * __bfloat162float(nw[c * 32 + d + 1]);
-          o[d] = x0 * c0 - x1 * s0;
-          o[d + 1] = x0 * s0 + x1 * c0;
+          const float co = h ? cs.z : cs.x, si = h ? cs.w : cs.y;
+          const float2 x = __fmul2_rn(__fmul2_rn(acc2(v, p + h), rs2), f2(w[d], w[d + 1]));
+          // (x0 c - x1 s, x1 c + x0 s)
+          const float2 r = __ffma2_rn(x, f2(co, co), __fmul2_rn(f2(x.y, x.x), f2(-si, si)));
+          o[d] = r.x;
+          o[d + 1] = r.y;
         }
       }
       store_row32(dst + c * 32, o);
@@ -345,7 +390,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const bool pf = ti.m_tile == 0;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (pf && kb + 8 < kblocks) pf_l2(&P.b_map[ti.p], (kb + 8) * KB, brow);
-          if (!mbar_wait(&empty[stage], phase ^ 1u, wc, kSiteEmpty)) {
+          if (!mbar_wait_sleep(&empty[stage], phase ^ 1u, wc, kSiteEmpty)) {
             ok = false;
             break;
           }
@@ -379,6 +424,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer (leader only)
     if (lane == 0 && rank == 0) {
       const uint32_t idesc = kFp8 ? make_idesc_e4m3(PAIR_M, BN) : make_idesc_bf16(PAIR_M, BN, false);
+      const uint64_t a_desc0 = make_sdesc_sw128(smem_u32(sA), 16, 1024);
+      const uint64_t b_desc0 = make_sdesc_sw128(smem_u32(sB), 16, 1024);
       uint32_t stage = 0, phase = 0;
       int local = 0;
       bool ok = true;
@@ -399,16 +446,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a_base = smem_u32(sA + stage * kATileBytes);
-          const uint32_t b_base = smem_u32(sB + stage * kBTileBytes);
+          const uint64_t ad = desc_advance(a_desc0, stage * (kATileBytes >> 4));
+          const uint64_t bd = desc_advance(b_desc0, stage * (kBTileBytes >> 4));
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {  // 32 bytes of K per MMA: 16 bf16 or 32 e4m3
-            const uint64_t ad = make_sdesc_sw128(a_base + kk * 32, 16, 1024);
-            const uint64_t bd = make_sdesc_sw128(b_base + kk * 32, 16, 1024);
             if (kFp8)
-              umma2_f8(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+              umma2_f8(d_tmem, desc_advance(ad, kk * 2), desc_advance(bd, kk * 2), idesc, (kb | kk) != 0 ? 1u : 0u);
             else
-              umma2(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+              umma2(d_tmem, desc_advance(ad, kk * 2), desc_advance(bd, kk * 2), idesc, (kb | kk) != 0 ? 1u : 0u);
           }
           commit_both(&empty[stage]);
           if (++stage == kStages) {
@@ -433,7 +478,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     int local = 0;
     for (int t = pair; t < P.total_tiles; t += npairs, ++local) {
       const int acc = local & 1;
-      bool ok = mbar_wait(&acc_full[acc], (uint32_t)(local >> 1) & 1u, wc, kSiteAccFull);
+      bool ok = mbar_wait_sleep(&acc_full[acc], (uint32_t)(local >> 1) & 1u, wc, kSiteAccFull);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
@@ -465,13 +510,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               if (pr.res_f32) load_row32_f32(pr.res_f32 + off + c * 32, xr);
               else load_row32(pr.res + off + c * 32, xr);
               if (pr.coef) {
+                const float2 g2 = f2(gsc, gsc);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) o[i] = xr[i] + gsc * __uint_as_float(v[i]);
+                for (int i = 0; i < 16; ++i) {
+                  const float2 r = __ffma2_rn(g2, acc2(v, i), f2(xr[2 * i], xr[2 * i + 1]));
+                  o[2 * i] = r.x;
+                  o[2 * i + 1] = r.y;
+                }
               } else {
                 float gv[32];
                 load_row32(grow + c * 32, gv);  // 16-byte loads of the gate vector
 #pragma unroll
-                for (int i = 0; i < 32; ++i) o[i] = xr[i] + gv[i] * __uint_as_float(v[i]);
+                for (int i = 0; i < 16; ++i) {
+                  const float2 r = __ffma2_rn(f2(gv[2 * i], gv[2 * i + 1]), acc2(v, i), f2(xr[2 * i], xr[2 * i + 1]));
+                  o[2 * i] = r.x;
+                  o[2 * i + 1] = r.y;
+                }
               }
             } else {
 #pragma unroll
