@@ -4,12 +4,17 @@
 // (sequence length not a multiple of 128) are masked out, padded tail queries not stored.
 //
 // One CTA per (pair of 128-query tiles, head, batch row), 320 threads:
-//   warp 0      TMA: Q0, Q1 once; K_j and V_j (128 keys x 128 dims as two 64-dim halves,
-//               128-byte swizzle) into 2-stage rings with separate full/empty barriers;
+//   warp 0      TMA: Q0, Q1 and K_0 once; then per key block j one ring slot (two slots)
+//               holding V_j and K_{j+1} (128 keys x 128 dims as two 64-dim halves, 128-byte
+//               swizzle) behind a single barrier, so that the MMA thread waits once per block;
 //   warp 1      tcgen05.mma from one thread, in the order
 //                 S0 = Q0 K_0^T, S1 = Q1 K_0^T, then for every key block j:
 //                 O0 += P0 V_j, S0 = Q0 K_{j+1}^T, O1 += P1 V_j, S1 = Q1 K_{j+1}^T,
-//               so that one tile's softmax overlaps the other tile's MMAs;
+//               so that one tile's softmax overlaps the other tile's MMAs.  Its only
+//               commits are the two "S_t ready" signals per block: a ring slot is released
+//               by a softmax thread of tile 1 once it sees S1 of the next block (every MMA
+//               reading the slot was issued before it), which saves the issuer a commit per
+//               slot -- on sm_103a an issuing thread is held ~one MMA time per commit;
 //   warps 2-5   softmax of tile 0, warps 6-9 softmax of tile 1: one thread per query row,
 //               S row streamed from TMEM in 32-key chunks, exp2 against the running
 //               maximum with log2(e)/sqrt(d) folded in, P rounded to bf16 and written back
@@ -124,9 +129,7 @@ __device__ __forceinline__ void softmax_row(uint32_t tS, int kv_valid, float c, 
   psum = ps0 + ps1;
 }
 
-enum : uint32_t {
-  kSiteQ = 0x201, kSiteKEmpty, kSiteVEmpty, kSiteKFull, kSitePFull, kSiteVFull, kSiteSFull, kSiteODone
-};
+enum : uint32_t { kSiteQ = 0x201, kSiteFree, kSiteReady, kSitePFull, kSiteSFull, kSiteODone };
 
 
 // Shared-memory descriptors of every MMA operand, computed once: Q_t (A of S_t = Q_t K^T),
@@ -147,50 +150,79 @@ __device__ __forceinline__ void make_descs(uint8_t* smem, Descs& d) {
     }
 }
 
+// Eight back-to-back MMAs (K = 128) from one asm statement: D = A B (first) then D += A B.
+__device__ __forceinline__ void umma8_ss(uint32_t d, const uint64_t (&a)[8], const uint64_t (&b)[8], uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred pf, pt;\n\t"
+      "setp.ne.b32 pf, %18, %18;\n\t"
+      "setp.eq.b32 pt, %18, %18;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %9, %17, pf;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %10, %17, pt;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %11, %17, pt;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %12, %17, pt;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %13, %17, pt;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %6, %14, %17, pt;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %15, %17, pt;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %8, %16, %17, pt;\n\t}" ::"r"(d),
+      "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(a[4]), "l"(a[5]), "l"(a[6]), "l"(a[7]), "l"(b[0]), "l"(b[1]),
+      "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]), "r"(idesc), "r"(0)
+      : "memory");
+}
+
+// Eight MMAs with A read from TMEM at columns a_tmem + 8 kk: D (+)= A B.
+__device__ __forceinline__ void umma8_ts(uint32_t d, uint32_t a_tmem, const uint64_t (&b)[8], uint32_t idesc,
+                                         uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred pa, pt;\n\t.reg .b32 t1, t2, t3, t4, t5, t6, t7;\n\t"
+      "setp.ne.b32 pa, %11, 0;\n\t"
+      "setp.eq.b32 pt, %11, %11;\n\t"
+      "add.u32 t1, %1, 8;\n\tadd.u32 t2, %1, 16;\n\tadd.u32 t3, %1, 24;\n\tadd.u32 t4, %1, 32;\n\t"
+      "add.u32 t5, %1, 40;\n\tadd.u32 t6, %1, 48;\n\tadd.u32 t7, %1, 56;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %10, pa;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t1], %3, %10, pt;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t2], %4, %10, pt;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t3], %5, %10, pt;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t4], %6, %10, pt;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t5], %7, %10, pt;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t6], %8, %10, pt;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t7], %9, %10, pt;\n\t}" ::"r"(d),
+      "r"(a_tmem), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]), "r"(idesc),
+      "r"(acc)
+      : "memory");
+}
+
 // S_t = Q_t K^T (K from ring stage ST), then arrive on `bar` when done.
 template <int ST>
 __device__ __forceinline__ void issue_qk(const Descs& d, uint32_t tmem, int t, uint32_t idesc, uint64_t* bar) {
-  const uint32_t tS = tmem + (uint32_t)(t * 256);
-#pragma unroll
-  for (int kk = 0; kk < 8; ++kk) umma_bf16(tS, d.q[t][kk], d.k[ST][kk], idesc, kk > 0 ? 1u : 0u);
+  umma8_ss(tmem + (uint32_t)(t * 256), d.q[t], d.k[ST], idesc);
   umma_commit(bar);
 }
 
 // O_t (+)= P_t V (V from ring stage ST), P_t read from TMEM over S_t.
 template <int ST>
 __device__ __forceinline__ void issue_pv(const Descs& d, uint32_t tmem, int t, bool acc, uint32_t idesc) {
-  const uint32_t tP = tmem + (uint32_t)(t * 256);
-  const uint32_t tO = tmem + (uint32_t)(t * 256 + 128);
-#pragma unroll
-  for (int kk = 0; kk < 8; ++kk) umma_bf16_ts(tO, tP + kk * 8, d.v[ST][kk], idesc, (acc || kk > 0) ? 1u : 0u);
+  umma8_ts(tmem + (uint32_t)(t * 256 + 128), tmem + (uint32_t)(t * 256), d.v[ST], idesc, acc ? 1u : 0u);
 }
 
-// One key block j (ring stage ST = j & 1) of the MMA issuer:
+// One key block j (ring stage ST = j & 1) of the MMA issuer, once V_j and K_{j+1} have
+// landed (one barrier for both):
 //   O0 += P0 V_j, S0 = Q0 K_{j+1}^T, O1 += P1 V_j, S1 = Q1 K_{j+1}^T.
 template <int ST>
 __device__ __forceinline__ bool mma_block(const Descs& d, uint32_t tmem, int j, int nkv, uint32_t idesc_qk,
-                                          uint32_t idesc_pv, uint64_t* k_full, uint64_t* k_empty, uint64_t* v_full,
-                                          uint64_t* v_empty, uint64_t* s_full, uint64_t* p_full, const WaitCtx& wc) {
+                                          uint32_t idesc_pv, uint64_t* ready, uint64_t* s_full, uint64_t* p_full,
+                                          const WaitCtx& wc) {
   constexpr int NST = ST ^ 1;
   const bool more = j + 1 < nkv;
-  if (!mbar_wait(&v_full[ST], (uint32_t)(j >> 1) & 1u, wc, kSiteVFull) ||
+  if (!mbar_wait(&ready[ST], (uint32_t)(j >> 1) & 1u, wc, kSiteReady) ||
       !mbar_wait(&p_full[0], (uint32_t)j & 1u, wc, kSitePFull))
     return false;
   tc_fence_after();
   issue_pv<ST>(d, tmem, 0, j > 0, idesc_pv);
-  if (more) {
-    if (!mbar_wait(&k_full[NST], (uint32_t)((j + 1) >> 1) & 1u, wc, kSiteKFull)) return false;
-    tc_fence_after();
-    issue_qk<NST>(d, tmem, 0, idesc_qk, &s_full[0]);
-  }
+  if (more) issue_qk<NST>(d, tmem, 0, idesc_qk, &s_full[0]);
   if (!mbar_wait(&p_full[1], (uint32_t)j & 1u, wc, kSitePFull)) return false;
   tc_fence_after();
   issue_pv<ST>(d, tmem, 1, j > 0, idesc_pv);
-  umma_commit(&v_empty[ST]);
-  if (more) {
-    issue_qk<NST>(d, tmem, 1, idesc_qk, &s_full[1]);
-    umma_commit(&k_empty[NST]);
-  }
+  if (more) issue_qk<NST>(d, tmem, 1, idesc_qk, &s_full[1]);
   return true;
 }
 
@@ -198,16 +230,14 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  uint64_t* q_full = bars + 0;
-  uint64_t* k_full = bars + 1;   // [2]
-  uint64_t* k_empty = bars + 3;  // [2]
-  uint64_t* v_full = bars + 5;   // [2]
-  uint64_t* v_empty = bars + 7;  // [2]
-  uint64_t* s_full = bars + 9;   // [2] per tile
-  uint64_t* p_full = bars + 11;  // [2] per tile
-  uint64_t* o_done = bars + 13;
-  uint64_t* drain = bars + 14;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  uint64_t* q_full = bars + 0;   // Q0, Q1 and K_0
+  uint64_t* ready = bars + 1;    // [2] ring slot: V_j and K_{j+1} landed
+  uint64_t* slot_free = bars + 3;  // [2] ring slot: every MMA reading V_j and K_{j+1} done
+  uint64_t* s_full = bars + 5;   // [2] per tile
+  uint64_t* p_full = bars + 7;   // [2] per tile
+  uint64_t* o_done = bars + 9;
+  uint64_t* drain = bars + 10;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -220,10 +250,8 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&k_full[i], 1);
-      mbar_init(&k_empty[i], 1);
-      mbar_init(&v_full[i], 1);
-      mbar_init(&v_empty[i], 1);
+      mbar_init(&ready[i], 1);
+      mbar_init(&slot_free[i], 1);
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 4);
     }
@@ -249,44 +277,43 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
+    // Ring slot b = j & 1 carries V_j (V stage b) and K_{j+1} (K stage (j+1) & 1).  Slot
+    // j (j >= 1) is loaded once S1 of block j - 1 is complete: that ends every read of the
+    // V_{j-2} and K_{j-1} it overwrites (for j = 1, of K_0 by the first two MMAs).
     if (lane == 0) {
-      int pending_k = 0, pending_v = 0;
+      int issued = 0;
       bool ok = true;
-      mbar_arrive_expect_tx(q_full, 2 * kTileBytes);
+      mbar_arrive_expect_tx(q_full, 3 * kTileBytes);
       for (int t = 0; t < 2; ++t) {
         tma_load_3d(smem + kOffQ + t * kTileBytes, &P.q_map, q_full, 0, q0 + t * kBQ, bh);
         tma_load_3d(smem + kOffQ + t * kTileBytes + kHalfBytes, &P.q_map, q_full, 64, q0 + t * kBQ, bh);
       }
-      for (int j = 0; j < nkv && ok; ++j) {
-        const int st = j & 1;
-        const uint32_t ph = (uint32_t)(j >> 1) & 1u;
-        if (!mbar_wait(&k_empty[st], ph ^ 1u, wc, kSiteKEmpty)) {
+      tma_load_3d(smem + kOffK, &P.k_map, q_full, 0, 0, bh);
+      tma_load_3d(smem + kOffK + kHalfBytes, &P.k_map, q_full, 64, 0, bh);
+      for (int j = 0; j < nkv; ++j) {
+        const int b = j & 1;
+        if (j >= 1 && !mbar_wait_sleep(&slot_free[b], (uint32_t)((j - 1) >> 1) & 1u, wc, kSiteFree)) {
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(&k_full[st], kTileBytes);
-        tma_load_3d(smem + kOffK + st * kTileBytes, &P.k_map, &k_full[st], 0, j * kBKV, bh);
-        tma_load_3d(smem + kOffK + st * kTileBytes + kHalfBytes, &P.k_map, &k_full[st], 64, j * kBKV, bh);
-        pending_k = j + 1;
-        if (!mbar_wait(&v_empty[st], ph ^ 1u, wc, kSiteVEmpty)) {
-          ok = false;
-          break;
+        const bool k_next = j + 1 < nkv;
+        mbar_arrive_expect_tx(&ready[b], k_next ? 2 * kTileBytes : kTileBytes);
+        tma_load_3d(smem + kOffV + b * kTileBytes, &P.v_map, &ready[b], 0, j * kBKV, bh);
+        tma_load_3d(smem + kOffV + b * kTileBytes + kHalfBytes, &P.v_map, &ready[b], 64, j * kBKV, bh);
+        if (k_next) {
+          const int kb = (j + 1) & 1;
+          tma_load_3d(smem + kOffK + kb * kTileBytes, &P.k_map, &ready[b], 0, (j + 1) * kBKV, bh);
+          tma_load_3d(smem + kOffK + kb * kTileBytes + kHalfBytes, &P.k_map, &ready[b], 64, (j + 1) * kBKV, bh);
         }
-        mbar_arrive_expect_tx(&v_full[st], kTileBytes);
-        tma_load_3d(smem + kOffV + st * kTileBytes, &P.v_map, &v_full[st], 0, j * kBKV, bh);
-        tma_load_3d(smem + kOffV + st * kTileBytes + kHalfBytes, &P.v_map, &v_full[st], 64, j * kBKV, bh);
-        pending_v = j + 1;
+        issued = j + 1;
       }
       if (!ok) {
         // Unwinding: let copies in flight land (bounded) before the block exits.
         const uint64_t t0 = global_timer_ns();
         while (!mbar_try(q_full, 0) && global_timer_ns() - t0 < 100000000ull) {
         }
-        for (int j = (pending_k > 2 ? pending_k - 2 : 0); j < pending_k; ++j)
-          while (!mbar_try(&k_full[j & 1], (uint32_t)(j >> 1) & 1u) && global_timer_ns() - t0 < 200000000ull) {
-          }
-        for (int j = (pending_v > 2 ? pending_v - 2 : 0); j < pending_v; ++j)
-          while (!mbar_try(&v_full[j & 1], (uint32_t)(j >> 1) & 1u) && global_timer_ns() - t0 < 300000000ull) {
+        for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j)
+          while (!mbar_try(&ready[j & 1], (uint32_t)(j >> 1) & 1u) && global_timer_ns() - t0 < 200000000ull) {
           }
       }
     }
@@ -297,18 +324,15 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
       const uint32_t idesc_pv = make_idesc_bf16(128, 128, true);
       Descs d;
       make_descs(smem, d);
-      bool ok = mbar_wait(q_full, 0, wc, kSiteQ) && mbar_wait(&k_full[0], 0, wc, kSiteKFull);
+      bool ok = mbar_wait(q_full, 0, wc, kSiteQ);
       if (ok) {
         tc_fence_after();
         issue_qk<0>(d, tmem, 0, idesc_qk, &s_full[0]);
         issue_qk<0>(d, tmem, 1, idesc_qk, &s_full[1]);
-        umma_commit(&k_empty[0]);
       }
       for (int j = 0; j < nkv && ok; j += 2) {
-        ok = mma_block<0>(d, tmem, j, nkv, idesc_qk, idesc_pv, k_full, k_empty, v_full, v_empty, s_full, p_full, wc);
-        if (ok && j + 1 < nkv)
-          ok = mma_block<1>(d, tmem, j + 1, nkv, idesc_qk, idesc_pv, k_full, k_empty, v_full, v_empty, s_full, p_full,
-                            wc);
+        ok = mma_block<0>(d, tmem, j, nkv, idesc_qk, idesc_pv, ready, s_full, p_full, wc);
+        if (ok && j + 1 < nkv) ok = mma_block<1>(d, tmem, j + 1, nkv, idesc_qk, idesc_pv, ready, s_full, p_full, wc);
       }
       umma_commit(o_done);
       umma_commit(drain);
@@ -331,6 +355,10 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
       ok = mbar_wait_sleep(&s_full[tile], (uint32_t)j & 1u, wc, kSiteSFull);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
+      // S1 of block j is complete, hence every MMA issued before it: the reads of V_{j-1}
+      // (V stage (j+1) & 1) and of K_j (K stage j & 1) are done, which is what the
+      // slot of key block j + 1 (V_{j+1}, K_{j+2}) overwrites.
+      if (tile == 1 && qq == 2 && lane == 0) mbar_arrive(&slot_free[(j + 1) & 1]);
       tc_fence_after();
       const int kv_valid = n - j * kBKV;
       // Fast path: exponentials against the running maximum, streamed over four
