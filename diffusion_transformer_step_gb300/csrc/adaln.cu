@@ -1,9 +1,14 @@
 // Adaptive LayerNorm with the per-step shift/scale: y = (1 + scale) LN(x) + shift.
 // LayerNorm over the hidden dim without affine, biased variance, fp32 statistics
 // (readings R3, R4).  Input rows are bf16, or fp32 for the dual-stream block's
-// intermediate residual stream.  One warp per row: 128-bit loads, the row kept in registers, a
-// two-pass mean / variance with warp-shuffle reductions.  HBM-bound: each row is read
-// once (2H bytes) and written once (2H bytes); the modulation vectors stay in L1/L2.
+// intermediate residual stream.  HBM-bound: each row is read once (2H or 4H bytes) and
+// written once (2H bytes, or H bytes + a scale in e4m3); the modulation vectors stay in L1.
+//
+// Persistent streaming: one CTA per SM slot, one warp per row at a time.  Each warp owns a
+// two-stage shared-memory ring: its lane 0 copies whole rows in with 1-D bulk copies
+// (cp.async.bulk, completing on the stage's mbarrier), so the next row is in flight while
+// the current one is reduced (two-pass mean / variance with warp shuffles, the row in
+// registers), modulated and stored with 16-byte stores.
 #include <cuda_fp8.h>
 
 #include "runtime.h"
@@ -12,109 +17,182 @@ namespace dit {
 
 namespace {
 
-constexpr int kRowsPerBlock = 8;  // 8 warps
+constexpr uint32_t kSiteAdaLN = 0x301;
+constexpr int kMaxWarps = 8;
+constexpr size_t kSmemBudget = 200 * 1024;
+
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
 
 // kFp8Out: y is written as e4m3 with one fp32 scale per row (y ~ scale * q, scale =
 // max|y| / 448, the largest finite e4m3), the A operand of an fp8 projection.
 template <int VPL, bool F32IN, bool kFp8Out>  // 8-element vectors per lane: hidden = VPL * 256
-__global__ void __launch_bounds__(kRowsPerBlock * 32) adaln_kernel(AdaLNArgs a) {
+__global__ void __launch_bounds__(kMaxWarps * 32, 1) adaln_kernel(AdaLNArgs a) {
+  constexpr int H = VPL * 256;
+  constexpr uint32_t kRowBytes = (uint32_t)H * (F32IN ? 4u : 2u);
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  __shared__ uint64_t bars[kMaxWarps][2];
+  __shared__ int abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long row = (long long)blockIdx.x * kRowsPerBlock + warp;
+  const int nwarps = blockDim.x >> 5;
+  uint8_t* buf0 = smem_raw + (size_t)(warp * 2) * kRowBytes;
+  uint8_t* buf1 = buf0 + kRowBytes;
+  uint64_t* bar = bars[warp];
   const long long total = (long long)a.batch * a.rows;
-  if (row >= total) return;
-  const int b = (int)(row / a.rows);
-  const int r = (int)(row - (long long)b * a.rows);
-  const int H = VPL * 256;
+  const long long stride = (long long)gridDim.x * nwarps;
+  long long r = (long long)blockIdx.x * nwarps + warp;
 
-  const long long xoff = b * a.x_bstride + (long long)(a.x_row0 + r) * H;
-  const uint4* xv = reinterpret_cast<const uint4*>(reinterpret_cast<const bf16*>(a.x) + xoff);
-  const float4* xf = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.x) + xoff);
-  uint4* yv = reinterpret_cast<uint4*>(a.y + b * a.y_bstride + (long long)r * H);
-  const bool lo = r < a.split;
-  const uint4* shv = reinterpret_cast<const uint4*>((lo ? a.shift_lo : a.shift_hi) + b * a.mod_stride);
-  const uint4* scv = reinterpret_cast<const uint4*>((lo ? a.scale_lo : a.scale_hi) + b * a.mod_stride);
+  if (lane == 0) {
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+  }
+  if (threadIdx.x == 0) abort_flag = 0;
+  fence_mbar_init();
+  __syncthreads();
+  const WaitCtx wc{a.status, &abort_flag, kWaitLimitNs};
 
-  float v[VPL][8];
-  float sum = 0.f;
+  auto row_src = [&](long long row) -> const uint8_t* {
+    const int b = (int)(row / a.rows);
+    const int rr = (int)(row - (long long)b * a.rows);
+    return reinterpret_cast<const uint8_t*>(a.x) +
+           (b * a.x_bstride + (long long)(a.x_row0 + rr) * H) * (F32IN ? 4 : 2);
+  };
+  long long issued = 0;  // rows copied in by this warp (lane 0's count)
+  if (lane == 0) {
+    for (int st = 0; st < 2; ++st) {
+      const long long row = r + st * stride;
+      if (row < total) {
+        mbar_arrive_expect_tx(&bar[st], kRowBytes);
+        bulk_copy_g2s(st ? buf1 : buf0, row_src(row), kRowBytes, &bar[st]);
+        ++issued;
+      }
+    }
+  }
+
+  long long consumed = 0;
+  for (int i = 0; r < total; ++i, r += stride) {
+    const int st = i & 1;
+    bool ok = mbar_wait(&bar[st], (uint32_t)(i >> 1) & 1u, wc, kSiteAdaLN);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) break;
+    const uint8_t* buf = st ? buf1 : buf0;
+    const int b = (int)(r / a.rows);
+    const int rw = (int)(r - (long long)b * a.rows);
+
+    float v[VPL][8];
+    float sum = 0.f;
 #pragma unroll
-  for (int i = 0; i < VPL; ++i) {
-    if (F32IN) {
-      const float4 f0 = __ldg(xf + 2 * (i * 32 + lane)), f1 = __ldg(xf + 2 * (i * 32 + lane) + 1);
-      v[i][0] = f0.x; v[i][1] = f0.y; v[i][2] = f0.z; v[i][3] = f0.w;
-      v[i][4] = f1.x; v[i][5] = f1.y; v[i][6] = f1.z; v[i][7] = f1.w;
+    for (int k = 0; k < VPL; ++k) {
+      if (F32IN) {
+        const float4* xf = reinterpret_cast<const float4*>(buf);
+        const float4 f0 = xf[2 * (k * 32 + lane)], f1 = xf[2 * (k * 32 + lane) + 1];
+        v[k][0] = f0.x; v[k][1] = f0.y; v[k][2] = f0.z; v[k][3] = f0.w;
+        v[k][4] = f1.x; v[k][5] = f1.y; v[k][6] = f1.z; v[k][7] = f1.w;
+      } else {
+        const uint4 u = reinterpret_cast<const uint4*>(buf)[k * 32 + lane];
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-      for (int j = 0; j < 8; ++j) sum += v[i][j];
-    } else {
-      const uint4 u = __ldg(xv + i * 32 + lane);
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        for (int j = 0; j < 4; ++j) {
+          const float2 f = unpack_bf16x2(w[j]);
+          v[k][2 * j] = f.x;
+          v[k][2 * j + 1] = f.y;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) sum += v[k][j];
+    }
+    ++consumed;
+    // Every lane has its part of the row in registers: the stage may be refilled (the
+    // generic-proxy reads are ordered before the bulk copy's async-proxy writes).
+    __syncwarp();
+    if (lane == 0) {
+      fence_proxy_async_smem();
+      const long long nrow = r + 2 * stride;
+      if (nrow < total) {
+        mbar_arrive_expect_tx(&bar[st], kRowBytes);
+        bulk_copy_g2s(st ? buf1 : buf0, row_src(nrow), kRowBytes, &bar[st]);
+        ++issued;
+      }
+    }
+
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    const float mean = sum * (1.0f / H);
+    float sq = 0.f;
+#pragma unroll
+    for (int k = 0; k < VPL; ++k)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float d = v[k][j] - mean;
+        sq += d * d;
+      }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+    const float rstd = rsqrtf(sq * (1.0f / H) + a.eps);
+
+    const bool lo = rw < a.split;
+    const uint4* shv = reinterpret_cast<const uint4*>((lo ? a.shift_lo : a.shift_hi) + b * a.mod_stride);
+    const uint4* scv = reinterpret_cast<const uint4*>((lo ? a.scale_lo : a.scale_hi) + b * a.mod_stride);
+    float amax = 0.f;
+#pragma unroll
+    for (int k = 0; k < VPL; ++k) {
+      const uint4 sh = __ldg(shv + k * 32 + lane);
+      const uint4 sc = __ldg(scv + k * 32 + lane);
+      const uint32_t shw[4] = {sh.x, sh.y, sh.z, sh.w};
+      const uint32_t scw[4] = {sc.x, sc.y, sc.z, sc.w};
+      uint32_t o[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const float2 f = unpack_bf16x2(w[j]);
-        v[i][2 * j] = f.x;
-        v[i][2 * j + 1] = f.y;
-        sum += f.x + f.y;
+        const float2 s2 = unpack_bf16x2(shw[j]);
+        const float2 c2 = unpack_bf16x2(scw[j]);
+        const float y0 = (1.0f + c2.x) * ((v[k][2 * j] - mean) * rstd) + s2.x;
+        const float y1 = (1.0f + c2.y) * ((v[k][2 * j + 1] - mean) * rstd) + s2.y;
+        if (kFp8Out) {
+          v[k][2 * j] = y0;
+          v[k][2 * j + 1] = y1;
+          amax = fmaxf(amax, fmaxf(fabsf(y0), fabsf(y1)));
+        } else {
+          o[j] = pack_bf16x2(y0, y1);
+        }
       }
+      if (!kFp8Out) {
+        uint4* yv = reinterpret_cast<uint4*>(a.y + b * a.y_bstride + (long long)rw * H);
+        yv[k * 32 + lane] = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+    }
+    if (kFp8Out) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      const float scale = amax > 0.f ? amax / 448.0f : 1.0f;
+      const float inv = 1.0f / scale;
+      uint2* qv = reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(a.y_q) + b * a.y_bstride + (long long)rw * H);
+#pragma unroll
+      for (int k = 0; k < VPL; ++k) {
+        uint32_t w[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const __nv_fp8x2_storage_t q0 =
+              __nv_cvt_float2_to_fp8x2(make_float2(v[k][4 * h] * inv, v[k][4 * h + 1] * inv), __NV_SATFINITE, __NV_E4M3);
+          const __nv_fp8x2_storage_t q1 = __nv_cvt_float2_to_fp8x2(
+              make_float2(v[k][4 * h + 2] * inv, v[k][4 * h + 3] * inv), __NV_SATFINITE, __NV_E4M3);
+          w[h] = (uint32_t)q0 | ((uint32_t)q1 << 16);
+        }
+        qv[k * 32 + lane] = make_uint2(w[0], w[1]);
+      }
+      if (lane == 0) a.y_scale[(long long)b * a.rows + rw] = scale;
     }
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-  const float mean = sum * (1.0f / H);
-  float sq = 0.f;
-#pragma unroll
-  for (int i = 0; i < VPL; ++i)
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float d = v[i][j] - mean;
-      sq += d * d;
-    }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
-  const float rstd = rsqrtf(sq * (1.0f / H) + a.eps);
-
-  float amax = 0.f;
-#pragma unroll
-  for (int i = 0; i < VPL; ++i) {
-    const uint4 sh = __ldg(shv + i * 32 + lane);
-    const uint4 sc = __ldg(scv + i * 32 + lane);
-    const uint32_t shw[4] = {sh.x, sh.y, sh.z, sh.w};
-    const uint32_t scw[4] = {sc.x, sc.y, sc.z, sc.w};
-    uint32_t o[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float2 s2 = unpack_bf16x2(shw[j]);
-      const float2 c2 = unpack_bf16x2(scw[j]);
-      const float y0 = (1.0f + c2.x) * ((v[i][2 * j] - mean) * rstd) + s2.x;
-      const float y1 = (1.0f + c2.y) * ((v[i][2 * j + 1] - mean) * rstd) + s2.y;
-      if (kFp8Out) {
-        v[i][2 * j] = y0;
-        v[i][2 * j + 1] = y1;
-        amax = fmaxf(amax, fmaxf(fabsf(y0), fabsf(y1)));
-      } else {
-        o[j] = pack_bf16x2(y0, y1);
+  // After an early exit, let this warp's copies still in flight land (bounded) before the
+  // block's shared memory is released.
+  if (lane == 0) {
+    const uint64_t t0 = global_timer_ns();
+    for (long long k = consumed; k < issued; ++k)
+      while (!mbar_try(&bar[k & 1], (uint32_t)(k >> 1) & 1u) && global_timer_ns() - t0 < 100000000ull) {
       }
-    }
-    if (!kFp8Out) yv[i * 32 + lane] = make_uint4(o[0], o[1], o[2], o[3]);
-  }
-  if (kFp8Out) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const float scale = amax > 0.f ? amax / 448.0f : 1.0f;
-    const float inv = 1.0f / scale;
-    uint2* qv = reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(a.y_q) + b * a.y_bstride + (long long)r * H);
-#pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-      uint32_t w[2];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const __nv_fp8x2_storage_t lo =
-            __nv_cvt_float2_to_fp8x2(make_float2(v[i][4 * h] * inv, v[i][4 * h + 1] * inv), __NV_SATFINITE, __NV_E4M3);
-        const __nv_fp8x2_storage_t hi =
-            __nv_cvt_float2_to_fp8x2(make_float2(v[i][4 * h + 2] * inv, v[i][4 * h + 3] * inv), __NV_SATFINITE, __NV_E4M3);
-        w[h] = (uint32_t)lo | ((uint32_t)hi << 16);
-      }
-      qv[i * 32 + lane] = make_uint2(w[0], w[1]);
-    }
-    if (lane == 0) a.y_scale[(long long)b * a.rows + r] = scale;
   }
 }
 
@@ -144,18 +222,33 @@ __global__ void quantize_rows_kernel(const bf16* __restrict__ w, int cols, uint8
   if (threadIdx.x == 0) scale[r] = s;
 }
 
+template <int VPL, bool F32IN, bool kFp8Out>
+cudaError_t launch_kind(const AdaLNArgs& a, cudaStream_t s) {
+  const size_t row_bytes = (size_t)VPL * 256 * (F32IN ? 4 : 2);
+  int warps = (int)(kSmemBudget / (2 * row_bytes));
+  if (warps > kMaxWarps) warps = kMaxWarps;
+  const size_t smem = (size_t)warps * 2 * row_bytes;
+  // One CTA per SM (the row in registers leaves room for one 256-thread CTA): 8 warps x 2
+  // rows in flight per SM cover the HBM latency.
+  const long long total = (long long)a.batch * a.rows;
+  long long grid = (total + warps - 1) / warps;
+  const long long cap = (long long)sm_count();
+  if (grid > cap) grid = cap;
+  auto k = adaln_kernel<VPL, F32IN, kFp8Out>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  LaunchScope scope(kClsAdaLN, s);
+  k<<<(unsigned)grid, warps * 32, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
 template <int VPL>
 cudaError_t launch_vpl(const AdaLNArgs& a, cudaStream_t s) {
-  const long long total = (long long)a.batch * a.rows;
-  const unsigned grid = (unsigned)((total + kRowsPerBlock - 1) / kRowsPerBlock);
-  LaunchScope scope(kClsAdaLN, s);
-  if (a.y_q)
-    adaln_kernel<VPL, false, true><<<grid, kRowsPerBlock * 32, 0, s>>>(a);
-  else if (a.x_f32)
-    adaln_kernel<VPL, true, false><<<grid, kRowsPerBlock * 32, 0, s>>>(a);
-  else
-    adaln_kernel<VPL, false, false><<<grid, kRowsPerBlock * 32, 0, s>>>(a);
-  return cudaGetLastError();
+  if (a.y_q) return launch_kind<VPL, false, true>(a, s);
+  if (a.x_f32) return launch_kind<VPL, true, false>(a, s);
+  return launch_kind<VPL, false, false>(a, s);
 }
 
 }  // namespace

@@ -248,6 +248,7 @@ dit_status run_dual_block(const dit_weights* w, int layer, const dit_shape* s, b
   // 1. y = adaLN(x) with each stream's attention shift / scale
   AdaLNArgs a1{B, N, H, x, 0, (long long)N * H, 0, y, (long long)N * H, n_txt,
                slot(kTxt, kShiftA), slot(kTxt, kScaleA), slot(kImg, kShiftA), slot(kImg, kScaleA), ms, c.eps};
+  a1.status = dst;
   DIT_CUDA(launch_adaln(a1, st));
 
   // 2. per-stream QKV projection + QK-RMSNorm + RoPE, head-major Q/K/V
@@ -282,6 +283,7 @@ dit_status run_dual_block(const dit_weights* w, int layer, const dit_shape* s, b
   // 5. y = adaLN(x1) with each stream's MLP shift / scale
   AdaLNArgs a2{B, N, H, x1, 1, (long long)N * H, 0, y, (long long)N * H, n_txt,
                slot(kTxt, kShiftM), slot(kTxt, kScaleM), slot(kImg, kShiftM), slot(kImg, kScaleM), ms, c.eps};
+  a2.status = dst;
   DIT_CUDA(launch_adaln(a2, st));
 
   // 6. act = silu(y Wg^T) * (y Wu^T) -> cat[:, :, H:H+F], per stream
@@ -325,6 +327,7 @@ dit_status run_single_block(const dit_weights* w, int layer, const dit_shape* s,
     a1.y_q = at(ws, L.yq);
     a1.y_scale = reinterpret_cast<float*>(at(ws, L.ascale));
   }
+  a1.status = dst;
   DIT_CUDA(launch_adaln(a1, st));
 
   GemmProblemHost p = blank_problem();
@@ -443,6 +446,7 @@ dit_status run_step_core(const dit_weights* w, const dit_shape* s, const bf16* i
   const bf16* fsc = mod + (long long)(kFinal + 1) * H;
   AdaLNArgs af{B, s->n_img, H, x, 0, (long long)N * H, s->n_txt, y, (long long)s->n_img * H, 0, fsh, fsc, fsh, fsc, ms,
                c.eps};
+  af.status = status_of(ws);
   DIT_CUDA(launch_adaln(af, st));
   p[0] = blank_problem();
   p[0].a = y; p[0].a_rows_total = s->n_img; p[0].lda = H; p[0].rows = s->n_img;

@@ -101,7 +101,7 @@ static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parit
     if ((i & 63u) == 63u) {
       if (*w.abort_flag) return false;
       if (global_timer_ns() - t0 > w.limit_ns) {
-        if (atomicOr(&w.status->word, kStatusTimeout) == 0u) atomicExch(&w.status->where, site);
+        if (w.status && atomicOr(&w.status->word, kStatusTimeout) == 0u) atomicExch(&w.status->where, site);
         *w.abort_flag = 1;
         __threadfence_block();
         return false;
@@ -140,7 +140,7 @@ static __device__ __noinline__ bool mbar_wait_sleep_slow(uint64_t* bar, uint32_t
     if (mbar_try_sleep(bar, parity)) return true;
     if (*w.abort_flag) return false;
     if (global_timer_ns() - t0 > w.limit_ns) {
-      if (atomicOr(&w.status->word, kStatusTimeout) == 0u) atomicExch(&w.status->where, site);
+      if (w.status && atomicOr(&w.status->word, kStatusTimeout) == 0u) atomicExch(&w.status->where, site);
       *w.abort_flag = 1;
       __threadfence_block();
       return false;

@@ -72,6 +72,9 @@ struct AdaLNArgs {
   // bytes (batch stride y_bstride) and one fp32 scale per row, y_scale [batch, rows].
   void* y_q;
   float* y_scale;
+  // Status word for the kernel's bounded waits (may be null: a wait that gives up then only
+  // ends the kernel early).
+  DeviceStatus* status = nullptr;
 };
 bool adaln_supports(int hidden);  // hidden / 256 in {1..6, 8, 10, 12, 14, 16}
 cudaError_t launch_adaln(const AdaLNArgs& a, cudaStream_t s);
