@@ -222,6 +222,68 @@ __global__ void quantize_rows_kernel(const bf16* __restrict__ w, int cols, uint8
   if (threadIdx.x == 0) scale[r] = s;
 }
 
+// Per-row e4m3 quantisation of activations (the A operand of an e4m3 out-projection):
+// row r of src (bf16, batch stride src_bstride, row stride ld, columns [col0, col0 + cols))
+// -> dst[r, :] (cols bytes, rows contiguous) and scale[r] = max|row| / 448.  One CTA per row,
+// the row held in registers (up to kMaxVec 8-element vectors per thread): one read, one write.
+constexpr int kQuantThreads = 256, kQuantMaxVec = 8;
+
+__global__ void __launch_bounds__(kQuantThreads) quantize_act_kernel(const bf16* __restrict__ src,
+                                                                     long long src_bstride, int ld, int col0, int rows,
+                                                                     int cols, uint8_t* __restrict__ dst,
+                                                                     float* __restrict__ scale) {
+  const long long row = blockIdx.x;  // batch * rows
+  const int b = (int)(row / rows);
+  const int r = (int)(row - (long long)b * rows);
+  const uint4* s4 = reinterpret_cast<const uint4*>(src + b * src_bstride + (long long)r * ld + col0);
+  const int nvec = cols >> 3;
+  uint4 v[kQuantMaxVec];
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < kQuantMaxVec; ++i) {
+    const int idx = threadIdx.x + i * kQuantThreads;
+    if (idx < nvec) {
+      v[i] = __ldg(s4 + idx);
+      const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 f = unpack_bf16x2(w[j]);
+        amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+      }
+    }
+  }
+  __shared__ float red[kQuantThreads / 32];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = red[0];
+#pragma unroll
+  for (int i = 1; i < kQuantThreads / 32; ++i) amax = fmaxf(amax, red[i]);
+  const float sc = amax > 0.f ? amax / 448.0f : 1.0f;
+  const float inv = 1.0f / sc;
+  uint2* d2 = reinterpret_cast<uint2*>(dst + row * cols);
+#pragma unroll
+  for (int i = 0; i < kQuantMaxVec; ++i) {
+    const int idx = threadIdx.x + i * kQuantThreads;
+    if (idx < nvec) {
+      const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+      uint32_t q[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float2 f0 = unpack_bf16x2(w[2 * h]), f1 = unpack_bf16x2(w[2 * h + 1]);
+        const __nv_fp8x2_storage_t q0 =
+            __nv_cvt_float2_to_fp8x2(make_float2(f0.x * inv, f0.y * inv), __NV_SATFINITE, __NV_E4M3);
+        const __nv_fp8x2_storage_t q1 =
+            __nv_cvt_float2_to_fp8x2(make_float2(f1.x * inv, f1.y * inv), __NV_SATFINITE, __NV_E4M3);
+        q[h] = (uint32_t)q0 | ((uint32_t)q1 << 16);
+      }
+      d2[idx] = make_uint2(q[0], q[1]);
+    }
+  }
+  if (threadIdx.x == 0) scale[row] = sc;
+}
+
 template <int VPL, bool F32IN, bool kFp8Out>
 cudaError_t launch_kind(const AdaLNArgs& a, cudaStream_t s) {
   const size_t row_bytes = (size_t)VPL * 256 * (F32IN ? 4 : 2);
@@ -246,7 +308,7 @@ cudaError_t launch_kind(const AdaLNArgs& a, cudaStream_t s) {
 
 template <int VPL>
 cudaError_t launch_vpl(const AdaLNArgs& a, cudaStream_t s) {
-  if (a.y_q) return launch_kind<VPL, false, true>(a, s);
+  if (a.y_q) return a.x_f32 ? launch_kind<VPL, true, true>(a, s) : launch_kind<VPL, false, true>(a, s);
   if (a.x_f32) return launch_kind<VPL, true, false>(a, s);
   return launch_kind<VPL, false, false>(a, s);
 }
@@ -286,6 +348,20 @@ cudaError_t launch_quantize_rows(const bf16* w, int rows, int cols, uint8_t* q, 
   if (rows <= 0) return cudaSuccess;
   LaunchScope scope(kClsPack, s);
   quantize_rows_kernel<<<rows, 256, 0, s>>>(w, cols, q, scale);
+  return cudaGetLastError();
+}
+}  // namespace dit
+
+namespace dit {
+bool quantize_act_supports(int cols) { return cols > 0 && cols % 16 == 0 && cols / 8 <= kQuantThreads * kQuantMaxVec; }
+
+cudaError_t launch_quantize_act(const bf16* src, long long src_bstride, int ld, int col0, int batch, int rows, int cols,
+                                uint8_t* dst, float* scale, cudaStream_t s) {
+  if ((long long)batch * rows == 0) return cudaSuccess;
+  if (!quantize_act_supports(cols)) return cudaErrorInvalidValue;
+  LaunchScope scope(kClsQuantAct, s);
+  quantize_act_kernel<<<(unsigned)((long long)batch * rows), kQuantThreads, 0, s>>>(src, src_bstride, ld, col0, rows,
+                                                                                    cols, dst, scale);
   return cudaGetLastError();
 }
 }  // namespace dit

@@ -32,7 +32,7 @@ const char* kernel_class_name(int cls) {
       "adaln",          "gemm_qkv_rmsnorm_rope", "gemm_fused_qkv_mlp",  "gemm_gated_residual",
       "gemm_swiglu",    "gemm_plain",            "attention",           "modulation_gemv",
       "rope_table",     "pack_mlp_in",           "gemm_dual_out_proj",  "gemm_dual_mlp_out",
-      "gemm_single_out_proj"};
+      "gemm_single_out_proj", "quantize_act"};
   return (cls >= 0 && cls < kClsCount) ? names[cls] : "?";
 }
 
@@ -145,7 +145,7 @@ dit_status check_shape(const dit_shape* s) {
 inline size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Layout {
-  size_t status, h1, h2, mod, x, x1, y, q, k, v, cat, yq, ascale;
+  size_t status, h1, h2, mod, x, x1, y, q, k, v, cat, yq, ascale, cq, cscale;
   size_t in_img, in_ref, in_txt, in_sigma, out_vel;
   size_t den_sigma, den_coef, den_mod, den_h1, den_h2, den_state, den_xbf;
   size_t block_end, step_end, total;
@@ -171,6 +171,8 @@ Layout layout(const dit_config& c, const dit_shape& s) {
   L.x1 = take(B * N * H * 4);
   L.yq = take(B * N * H);
   L.ascale = take(B * N * 4);
+  L.cq = take(B * N * (H + F));  // e4m3 input of an out-projection (attention output / activations)
+  L.cscale = take(B * N * 4);
   L.block_end = o;
   L.mod = take(B * 17 * H * 2);
   L.x = take(B * N * H * 2);
@@ -211,6 +213,27 @@ dit_status check_stream_weights(const dit_stream_weights& w) {
   return DIT_OK;
 }
 
+// e4m3 copies: a matrix is absent (q NULL) or both pointers are 16-byte aligned; the fused
+// single-stream projection is always present; a dual-block projection is given for both
+// streams or for neither.
+inline bool fp8_matrix_ok(const dit_fp8_matrix& m) { return !m.q || (aligned16(m.q) && aligned16(m.scale)); }
+
+dit_status check_single_fp8(const dit_config& c, const dit_single_fp8& f) {
+  if (!aligned16(f.qkv_mlp_q) || !aligned16(f.qkv_mlp_scale) || !fp8_matrix_ok(f.out)) return DIT_ERR_INVALID_ARG;
+  if (f.out.q && !quantize_act_supports(c.hidden + c.mlp_hidden)) return DIT_ERR_UNSUPPORTED;
+  return DIT_OK;
+}
+
+dit_status check_dual_fp8(const dit_config& c, const dit_dual_fp8& f) {
+  const dit_fp8_matrix* img[4] = {&f.img.qkv, &f.img.mlp_in, &f.img.out, &f.img.mlp_out};
+  const dit_fp8_matrix* txt[4] = {&f.txt.qkv, &f.txt.mlp_in, &f.txt.out, &f.txt.mlp_out};
+  for (int i = 0; i < 4; ++i)
+    if (!fp8_matrix_ok(*img[i]) || !fp8_matrix_ok(*txt[i]) || (img[i]->q == nullptr) != (txt[i]->q == nullptr))
+      return DIT_ERR_INVALID_ARG;
+  if ((f.img.out.q || f.img.mlp_out.q) && !quantize_act_supports(c.hidden + c.mlp_hidden)) return DIT_ERR_UNSUPPORTED;
+  return DIT_OK;
+}
+
 dit_status check_block_args(const dit_weights* w, const dit_shape* shape, const void* x, const void* mod,
                             const float* rope, void* ws, size_t ws_bytes) {
   if (!w) return DIT_ERR_INVALID_ARG;
@@ -244,10 +267,32 @@ dit_status run_dual_block(const dit_weights* w, int layer, const dit_shape* s, b
   DeviceStatus* dst = status_of(ws);
   const long long ms = 17LL * H;
   auto slot = [&](int base, int which) { return mod + (long long)(base + which) * H; };
+  // e4m3 projections (per kind, both streams or neither): inputs quantised per token row,
+  // by the adaLN kernel (QKV, MLP-in) or by a quantising pass over cat (out, MLP-out)
+  const dit_dual_fp8* f8 = w->dual_fp8 ? &w->dual_fp8[layer] : nullptr;
+  const dit_stream_fp8* sf[2] = {f8 ? &f8->txt : nullptr, f8 ? &f8->img : nullptr};  // order of sw below
+  const bool q_qkv = f8 && f8->img.qkv.q, q_in = f8 && f8->img.mlp_in.q;
+  const bool q_out = f8 && f8->img.out.q, q_mo = f8 && f8->img.mlp_out.q;
+  uint8_t* yq = at(ws, L.yq);
+  float* ascale = reinterpret_cast<float*>(at(ws, L.ascale));
+  uint8_t* cq = at(ws, L.cq);
+  float* cscale = reinterpret_cast<float*>(at(ws, L.cscale));
+  auto use_fp8 = [](GemmProblemHost& pp, const dit_fp8_matrix& m, const uint8_t* a8, const float* as, int lda) {
+    pp.fp8 = 1;
+    pp.a = reinterpret_cast<const bf16*>(a8);
+    pp.lda = lda;
+    pp.a_scale = as;
+    pp.w = reinterpret_cast<const bf16*>(m.q);
+    pp.w_scale = m.scale;
+  };
 
   // 1. y = adaLN(x) with each stream's attention shift / scale
   AdaLNArgs a1{B, N, H, x, 0, (long long)N * H, 0, y, (long long)N * H, n_txt,
                slot(kTxt, kShiftA), slot(kTxt, kScaleA), slot(kImg, kShiftA), slot(kImg, kScaleA), ms, c.eps};
+  if (q_qkv) {
+    a1.y_q = yq;
+    a1.y_scale = ascale;
+  }
   a1.status = dst;
   DIT_CUDA(launch_adaln(a1, st));
 
@@ -262,6 +307,7 @@ dit_status run_dual_block(const dit_weights* w, int layer, const dit_shape* s, b
     p[i].n_qkv = 3 * H; p[i].hidden = H; p[i].q = q; p[i].kk = k; p[i].v = v;
     p[i].q_norm = (const bf16*)sw[i]->q_norm; p[i].k_norm = (const bf16*)sw[i]->k_norm;
     p[i].rope = rope; p[i].seq = N; p[i].tok0 = row0[i];
+    if (q_qkv) use_fp8(p[i], sf[i]->qkv, yq, ascale, H);
   }
   DIT_CUDA(launch_gemm(p, 2, B, c.eps, dst, kClsGemmQKV, st));
 
@@ -271,18 +317,24 @@ dit_status run_dual_block(const dit_weights* w, int layer, const dit_shape* s, b
   // 4. x1 = x + gate_a * (attn out^T), per stream; x1 kept in fp32 so the block rounds
   //    the residual stream to bf16 once
   const int gate_a[2] = {kTxt + kGateA, kImg + kGateA};
+  if (q_out) DIT_CUDA(launch_quantize_act(cat, (long long)N * (H + F), H + F, 0, B, N, H, cq, cscale, st));
   for (int i = 0; i < 2; ++i) {
     p[i] = blank_problem();
     p[i].a = cat; p[i].a_rows_total = N; p[i].lda = H + F; p[i].a_row0 = row0[i]; p[i].rows = rows[i];
     p[i].w = (const bf16*)sw[i]->out; p[i].n = H; p[i].k = H; p[i].epi = kEpiResidual;
     p[i].res = x; p[i].out_f32 = x1; p[i].out_bstride = (long long)N * H; p[i].ld_out = H; p[i].out_row0 = row0[i];
     p[i].gate = mod + (long long)gate_a[i] * H; p[i].gate_stride = ms;
+    if (q_out) use_fp8(p[i], sf[i]->out, cq, cscale, H);
   }
   DIT_CUDA(launch_gemm(p, 2, B, c.eps, dst, kClsGemmDualOut, st));
 
   // 5. y = adaLN(x1) with each stream's MLP shift / scale
   AdaLNArgs a2{B, N, H, x1, 1, (long long)N * H, 0, y, (long long)N * H, n_txt,
                slot(kTxt, kShiftM), slot(kTxt, kScaleM), slot(kImg, kShiftM), slot(kImg, kScaleM), ms, c.eps};
+  if (q_in) {
+    a2.y_q = yq;
+    a2.y_scale = ascale;
+  }
   a2.status = dst;
   DIT_CUDA(launch_adaln(a2, st));
 
@@ -293,17 +345,20 @@ dit_status run_dual_block(const dit_weights* w, int layer, const dit_shape* s, b
     p[i].w = (const bf16*)sw[i]->mlp_in; p[i].n = 2 * F; p[i].k = H; p[i].epi = kEpiSwiGLU;
     p[i].out = cat; p[i].out_bstride = (long long)N * (H + F); p[i].ld_out = H + F; p[i].out_row0 = row0[i];
     p[i].out_col0 = H;
+    if (q_in) use_fp8(p[i], sf[i]->mlp_in, yq, ascale, H);
   }
   DIT_CUDA(launch_gemm(p, 2, B, c.eps, dst, kClsGemmSwiGLU, st));
 
   // 7. x = x1 + gate_m * (act mlp_out^T), per stream
   const int gate_m[2] = {kTxt + kGateM, kImg + kGateM};
+  if (q_mo) DIT_CUDA(launch_quantize_act(cat, (long long)N * (H + F), H + F, H, B, N, F, cq, cscale, st));
   for (int i = 0; i < 2; ++i) {
     p[i] = blank_problem();
     p[i].a = cat + H; p[i].a_rows_total = N; p[i].lda = H + F; p[i].a_row0 = row0[i]; p[i].rows = rows[i];
     p[i].w = (const bf16*)sw[i]->mlp_out; p[i].n = H; p[i].k = F; p[i].epi = kEpiResidual;
     p[i].res_f32 = x1; p[i].out = x; p[i].out_bstride = (long long)N * H; p[i].ld_out = H; p[i].out_row0 = row0[i];
     p[i].gate = mod + (long long)gate_m[i] * H; p[i].gate_stride = ms;
+    if (q_mo) use_fp8(p[i], sf[i]->mlp_out, cq, cscale, F);
   }
   DIT_CUDA(launch_gemm(p, 2, B, c.eps, dst, kClsGemmDualMlpOut, st));
   return DIT_OK;
@@ -351,6 +406,17 @@ dit_status run_single_block(const dit_weights* w, int layer, const dit_shape* s,
   p.w = (const bf16*)sw.out; p.n = H; p.k = H + F; p.epi = kEpiResidual;
   p.out = x; p.out_bstride = (long long)N * H; p.ld_out = H; p.out_row0 = 0;
   p.gate = mod + (long long)(kSingle + 2) * H; p.gate_stride = ms;
+  if (f8 && f8->out.q) {
+    // e4m3 out-projection: [attn | act] quantised per token row first
+    uint8_t* cq = at(ws, L.cq);
+    float* cscale = reinterpret_cast<float*>(at(ws, L.cscale));
+    DIT_CUDA(launch_quantize_act(cat, (long long)N * (H + F), H + F, 0, B, N, H + F, cq, cscale, st));
+    p.fp8 = 1;
+    p.a = reinterpret_cast<const bf16*>(cq);
+    p.a_scale = cscale;
+    p.w = reinterpret_cast<const bf16*>(f8->out.q);
+    p.w_scale = f8->out.scale;
+  }
   DIT_CUDA(launch_gemm(&p, 1, B, c.eps, dst, kClsGemmSingleOut, st));
   return DIT_OK;
 }
@@ -386,13 +452,13 @@ dit_status check_step_weights(const dit_weights* w) {
   for (int i = 0; i < w->cfg.n_dual; ++i) {
     DIT_TRY(check_stream_weights(w->dual[i].img));
     DIT_TRY(check_stream_weights(w->dual[i].txt));
+    if (w->dual_fp8) DIT_TRY(check_dual_fp8(w->cfg, w->dual_fp8[i]));
   }
   for (int i = 0; i < w->cfg.n_single; ++i) {
     const dit_single_weights& s = w->single[i];
     if (!aligned16(s.qkv_mlp) || !aligned16(s.q_norm) || !aligned16(s.k_norm) || !aligned16(s.out))
       return DIT_ERR_INVALID_ARG;
-    if (w->single_fp8 && (!aligned16(w->single_fp8[i].qkv_mlp_q) || !aligned16(w->single_fp8[i].qkv_mlp_scale)))
-      return DIT_ERR_INVALID_ARG;
+    if (w->single_fp8) DIT_TRY(check_single_fp8(w->cfg, w->single_fp8[i]));
   }
   return DIT_OK;
 }
@@ -596,6 +662,7 @@ dit_status dit_dual_block_fwd(const dit_weights* w, int layer, const dit_shape* 
   if (layer < 0 || layer >= w->cfg.n_dual || !w->dual) return DIT_ERR_INVALID_ARG;
   DIT_TRY(check_stream_weights(w->dual[layer].img));
   DIT_TRY(check_stream_weights(w->dual[layer].txt));
+  if (w->dual_fp8) DIT_TRY(check_dual_fp8(w->cfg, w->dual_fp8[layer]));
   return run_dual_block(w, layer, shape, (bf16*)x_dev, (const bf16*)mod_dev, rope_dev, ws, (cudaStream_t)stream);
 }
 
@@ -607,8 +674,7 @@ dit_status dit_single_block_fwd(const dit_weights* w, int layer, const dit_shape
   const dit_single_weights& s = w->single[layer];
   if (!aligned16(s.qkv_mlp) || !aligned16(s.q_norm) || !aligned16(s.k_norm) || !aligned16(s.out))
     return DIT_ERR_INVALID_ARG;
-  if (w->single_fp8 && (!aligned16(w->single_fp8[layer].qkv_mlp_q) || !aligned16(w->single_fp8[layer].qkv_mlp_scale)))
-    return DIT_ERR_INVALID_ARG;
+  if (w->single_fp8) DIT_TRY(check_single_fp8(w->cfg, w->single_fp8[layer]));
   return run_single_block(w, layer, shape, (bf16*)x_dev, (const bf16*)mod_dev, rope_dev, ws, (cudaStream_t)stream);
 }
 

@@ -25,7 +25,8 @@ enum KernelClass : int {
   kClsGemmDualOut = 10,    // dual-stream attention out-projection + gated residual
   kClsGemmDualMlpOut = 11, // dual-stream MLP-out + gated residual
   kClsGemmSingleOut = 12,  // single-stream out-projection over [attn | act] + gated residual
-  kClsCount = 13
+  kClsQuantAct = 13,       // per-row e4m3 quantisation of an out-projection's input
+  kClsCount = 14
 };
 
 const char* kernel_class_name(int cls);
@@ -80,6 +81,12 @@ bool adaln_supports(int hidden);  // hidden / 256 in {1..6, 8, 10, 12, 14, 16}
 cudaError_t launch_adaln(const AdaLNArgs& a, cudaStream_t s);
 // Per-row e4m3 quantisation of a bf16 weight [rows, cols]: q bytes, scale fp32 [rows].
 cudaError_t launch_quantize_rows(const bf16* w, int rows, int cols, uint8_t* q, float* scale, cudaStream_t s);
+// Per-row e4m3 quantisation of activations: rows of src (bf16; batch stride src_bstride,
+// row stride ld, columns [col0, col0 + cols)) -> dst [batch, rows, cols] bytes and
+// scale [batch * rows] = max|row| / 448.
+bool quantize_act_supports(int cols);  // cols % 16 == 0 and cols <= 16384
+cudaError_t launch_quantize_act(const bf16* src, long long src_bstride, int ld, int col0, int batch, int rows, int cols,
+                                uint8_t* dst, float* scale, cudaStream_t s);
 
 // y[b, n] = act(sum_k W[n, k] x[b, k]); x fp32 [batch, k]; W bf16 [n, k].
 // act: 0 none, 1 SiLU.  Output fp32 (y_f32) or bf16 (y_bf16), exactly one non-null.

@@ -50,14 +50,27 @@ class dit_single_weights(C.Structure):
     _fields_ = [(n, C.c_void_p) for n in ("qkv_mlp", "q_norm", "k_norm", "out")]
 
 
+class dit_fp8_matrix(C.Structure):
+    _fields_ = [("q", C.c_void_p), ("scale", C.c_void_p)]
+
+
 class dit_single_fp8(C.Structure):
-    _fields_ = [("qkv_mlp_q", C.c_void_p), ("qkv_mlp_scale", C.c_void_p)]
+    _fields_ = [("qkv_mlp_q", C.c_void_p), ("qkv_mlp_scale", C.c_void_p), ("out", dit_fp8_matrix)]
+
+
+class dit_stream_fp8(C.Structure):
+    _fields_ = [(n, dit_fp8_matrix) for n in ("qkv", "mlp_in", "out", "mlp_out")]
+
+
+class dit_dual_fp8(C.Structure):
+    _fields_ = [("img", dit_stream_fp8), ("txt", dit_stream_fp8)]
 
 
 class dit_weights(C.Structure):
     _fields_ = [("cfg", dit_config), ("mod", dit_mod_weights), ("x_emb", C.c_void_p), ("ctx_emb", C.c_void_p),
                 ("proj_out", C.c_void_p), ("dual", C.POINTER(dit_dual_weights)),
-                ("single", C.POINTER(dit_single_weights)), ("single_fp8", C.POINTER(dit_single_fp8))]
+                ("single", C.POINTER(dit_single_weights)), ("single_fp8", C.POINTER(dit_single_fp8)),
+                ("dual_fp8", C.POINTER(dit_dual_fp8))]
 
 
 _P = C.c_void_p
@@ -380,18 +393,36 @@ class DeviceWeights:
             s.out = dev(src["out"]).data_ptr()
         w.dual = C.cast(self._dual, C.POINTER(dit_dual_weights))
         w.single = C.cast(self._single, C.POINTER(dit_single_weights))
-        if fp8 and ns > 0:
-            # e4m3 copies of the fused single-stream projections (packed row order)
+        # e4m3 copies (the library's reading of the precision knob): fp8="fused" quantises only
+        # the single-stream fused QKV + MLP-in projections; fp8=True or "all" every block
+        # projection (dual QKV / MLP-in / out / MLP-out, single fused / out).
+        scope = {False: None, None: None, True: "all", "all": "all", "fused": "fused"}[fp8]
+
+        def quant(ptr, rows, cols):
+            q = torch.empty((rows, cols), dtype=torch.uint8, device=device)
+            sc = torch.empty((rows,), dtype=torch.float32, device=device)
+            dit_quantize_rows_fp8(ptr, rows, cols, q, sc)
+            keep.extend([q, sc])
+            return q.data_ptr(), sc.data_ptr()
+
+        if scope and ns > 0:
             self._single_fp8 = (dit_single_fp8 * ns)()
-            rows = 3 * H + 2 * F
             for i in range(ns):
-                q = torch.empty((rows, H), dtype=torch.uint8, device=device)
-                sc = torch.empty((rows,), dtype=torch.float32, device=device)
-                dit_quantize_rows_fp8(self._single[i].qkv_mlp, rows, H, q, sc)
-                keep += [q, sc]
-                self._single_fp8[i].qkv_mlp_q = q.data_ptr()
-                self._single_fp8[i].qkv_mlp_scale = sc.data_ptr()
+                f8 = self._single_fp8[i]
+                f8.qkv_mlp_q, f8.qkv_mlp_scale = quant(self._single[i].qkv_mlp, 3 * H + 2 * F, H)
+                if scope == "all":
+                    f8.out.q, f8.out.scale = quant(self._single[i].out, H, H + F)
             w.single_fp8 = C.cast(self._single_fp8, C.POINTER(dit_single_fp8))
+        if scope == "all" and nd > 0:
+            self._dual_fp8 = (dit_dual_fp8 * nd)()
+            for i in range(nd):
+                for side in ("img", "txt"):
+                    sw, f8 = getattr(self._dual[i], side), getattr(self._dual_fp8[i], side)
+                    f8.qkv.q, f8.qkv.scale = quant(sw.qkv, 3 * H, H)
+                    f8.mlp_in.q, f8.mlp_in.scale = quant(sw.mlp_in, 2 * F, H)
+                    f8.out.q, f8.out.scale = quant(sw.out, H, H)
+                    f8.mlp_out.q, f8.mlp_out.scale = quant(sw.mlp_out, H, F)
+            w.dual_fp8 = C.cast(self._dual_fp8, C.POINTER(dit_dual_fp8))
         self.w = w
         self._keep = keep
         torch.cuda.synchronize()

@@ -99,24 +99,47 @@ typedef struct {
   const void *qkv_mlp, *q_norm, *k_norm, *out;
 } dit_single_weights;
 
-/* Low-precision copy of a single-stream block's fused projection (the "dit_prec" precision
- * knob of the "tt_flux2_klein -- Python reference" KleinTT constructor): qkv_mlp_q
- * [3H + 2F, H] e4m3 bytes in the same (packed) row order as qkv_mlp, and qkv_mlp_scale
- * [3H + 2F] fp32, one per output row, with qkv_mlp ~= scale[n] * q[n, :] (from
- * dit_quantize_rows_fp8). */
+/* Low-precision (e4m3) copy of one projection matrix W [rows, cols]: q [rows, cols] e4m3
+ * bytes in the same row order as W and scale [rows] fp32, one per output row, with
+ * W ~= scale[n] * q[n, :] (from dit_quantize_rows_fp8).  q == NULL means "this projection
+ * stays bf16".  The "dit_prec" precision knob of the "tt_flux2_klein -- Python reference"
+ * KleinTT constructor names a precision choice for the projections without fixing a format;
+ * e4m3 with per-row scales is this library's reading of it. */
+typedef struct {
+  const void* q;
+  const float* scale;
+} dit_fp8_matrix;
+
+/* e4m3 copies of a single-stream block's projections: the fused QKV + MLP-in [3H + 2F, H]
+ * (packed row order of qkv_mlp; both pointers required) and, optionally, the
+ * out-projection [H, H + F] (out.q NULL: bf16). */
 typedef struct {
   const void* qkv_mlp_q;
   const float* qkv_mlp_scale;
+  dit_fp8_matrix out;
 } dit_single_fp8;
+
+/* e4m3 copies of one stream's projections in a dual-stream block: qkv [3H, H], mlp_in
+ * [2F, H] (packed row order), out [H, H], mlp_out [H, F].  Each projection runs in e4m3
+ * when BOTH streams give its copy and in bf16 when neither does (the two streams share one
+ * launch); one stream alone is an argument error. */
+typedef struct {
+  dit_fp8_matrix qkv, mlp_in, out, mlp_out;
+} dit_stream_fp8;
+typedef struct {
+  dit_stream_fp8 img, txt;
+} dit_dual_fp8;
 
 /* All weights.  `dual` and `single` are HOST arrays of n_dual and n_single entries
  * (they hold device pointers); they must stay valid for the duration of each call.
  * x_emb [H, in_channels], ctx_emb [H, txt_dim], proj_out [in_channels, H].
- * single_fp8: NULL for the bf16 path; else a HOST array of n_single entries, and every
- * single-stream block runs its fused QKV + MLP-in projection in e4m3 (the modulated
- * activations are quantised per token row by the adaLN kernel, the product is
- * dequantised in the GEMM epilogue before RMSNorm / RoPE / SwiGLU); everything else
- * stays bf16. */
+ * single_fp8 / dual_fp8: NULL for the bf16 path; else HOST arrays of n_single / n_dual
+ * entries naming e4m3 copies of the block projections.  An e4m3 projection takes its input
+ * quantised per token row (scale = max|row| / 448): the modulated activations by the adaLN
+ * kernel, the attention output and the SwiGLU activations by a quantising pass before the
+ * out-projections; the product is accumulated in fp32 and dequantised in the GEMM epilogue
+ * before RMSNorm / RoPE / SwiGLU / the gated residual.  Attention, norms, modulation,
+ * embedders and the final projection stay bf16. */
 typedef struct {
   dit_config cfg;
   dit_mod_weights mod;
@@ -124,6 +147,7 @@ typedef struct {
   const dit_dual_weights* dual;
   const dit_single_weights* single;
   const dit_single_fp8* single_fp8;
+  const dit_dual_fp8* dual_fp8;
 } dit_weights;
 
 /* Human-readable name of a status code (static string, never NULL). */

@@ -121,6 +121,48 @@ def test_invalid_arguments_rejected_before_any_launch(dit):
     assert dit.dit_launch_count() == before
 
 
+def test_fp8_copies_are_validated_before_launch(dit):
+    """e4m3 copies: a dual-block projection given for one stream only, a missing or
+    misaligned scale, are refused before any launch (readings of the precision knob)."""
+    L = dit.lib()
+    before = dit.dit_launch_count()
+    c = dit.dit_config_klein()
+    c.n_dual, c.n_single = 1, 1
+    shape = dit.make_shape(1, 512, 4096, 0)
+    fake = 0x10000  # aligned, never dereferenced: the fp8 checks fail first
+    dual = (dit.dit_dual_weights * 1)()
+    for side in ("img", "txt"):
+        sw = getattr(dual[0], side)
+        for n in ("qkv", "q_norm", "k_norm", "out", "mlp_in", "mlp_out"):
+            setattr(sw, n, fake)
+    single = (dit.dit_single_weights * 1)()
+    for n in ("qkv_mlp", "q_norm", "k_norm", "out"):
+        setattr(single[0], n, fake)
+    w = dit.dit_weights()
+    w.cfg = c
+    w.dual = C.cast(dual, C.POINTER(dit.dit_dual_weights))
+    w.single = C.cast(single, C.POINTER(dit.dit_single_weights))
+    d8 = (dit.dit_dual_fp8 * 1)()
+    d8[0].img.qkv.q, d8[0].img.qkv.scale = fake, fake  # the text stream's copy is missing
+    w.dual_fp8 = C.cast(d8, C.POINTER(dit.dit_dual_fp8))
+    args = (C.byref(shape), fake, fake, fake, fake, 1 << 40, None)
+    assert L.dit_dual_block_fwd(C.byref(w), 0, *args) == dit.DIT_ERR_INVALID_ARG
+    d8[0].txt.qkv.q, d8[0].txt.qkv.scale = fake, fake + 4  # misaligned scale
+    assert L.dit_dual_block_fwd(C.byref(w), 0, *args) == dit.DIT_ERR_INVALID_ARG
+    d8[0].txt.qkv.scale = fake
+    s8 = (dit.dit_single_fp8 * 1)()
+    s8[0].qkv_mlp_q, s8[0].qkv_mlp_scale = fake, fake
+    s8[0].out.q = fake  # out-projection copy without its scales
+    w.single_fp8 = C.cast(s8, C.POINTER(dit.dit_single_fp8))
+    assert L.dit_single_block_fwd(C.byref(w), 0, *args) == dit.DIT_ERR_INVALID_ARG
+    assert L.dit_step_fwd(C.byref(w), C.byref(shape), fake, None, fake, fake, fake, fake, fake, 1 << 40,
+                          None) == dit.DIT_ERR_INVALID_ARG
+    s8[0].qkv_mlp_q = None  # the fused projection's copy is required once single_fp8 is given
+    s8[0].out.scale = fake
+    assert L.dit_single_block_fwd(C.byref(w), 0, *args) == dit.DIT_ERR_INVALID_ARG
+    assert dit.dit_launch_count() == before
+
+
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch, dit):
     import importlib
     mod = importlib.reload(dit)

@@ -18,10 +18,11 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 BLOCK_ATOL, BLOCK_COS, STEP_COS = 3e-2, 0.999, 0.995
 # e4m3 keeps 3 mantissa bits (relative rounding up to 2^-4, rms 2^-4/sqrt(3) per operand):
-# each product of two quantised operands carries ~5 % rms relative error, so the fused
-# projection's outputs do too.  Measured on GB300: 1024^2 single block max-abs 0.116,
-# update-cosine 0.9984; tiny block update-cosine 0.983 (its small update is also quantised
-# by the bf16 output).  Bars at about twice those errors; the bf16 path keeps 3e-2.
+# each product of two quantised operands carries ~5 % rms relative error, so the
+# projections' outputs do too.  Measured on GB300 with every block projection in e4m3:
+# 1024^2 single and dual blocks max-abs 0.139, update-cosine 0.9977; tiny blocks
+# update-cosine 0.977-0.979 (their small updates are also quantised by the bf16 output);
+# full 1024^2 step cosine 0.990.  Bars at about twice those errors; bf16 keeps 3e-2.
 FP8_BLOCK_ATOL, FP8_UPDATE_COS, FP8_STEP_COS = 0.25, 0.97, 0.98
 
 TINY_REF = synth.Workload("tiny_ref_b2", synth.TINY, 2, 40, (7, 20), ((6, 10),))       # N = 240, ragged
@@ -168,7 +169,7 @@ def test_step_host_buffers_match_device_buffers(dit):
 
 def test_step_klein_1024(dit):
     """The full 25-block step at 1024x1024 against the fp32 oracle (about a minute of CPU),
-    in bf16 and with the e4m3 single-stream projections."""
+    in bf16 and with every block projection in e4m3."""
     wl = synth.WORKLOADS["step_1024"]
     logical = synth.model_weights(wl.widths, seed=0)
     inp = synth.step_inputs(wl, seed=0)
@@ -179,7 +180,7 @@ def test_step_klein_1024(dit):
     want = _oracle_step(wl, logical, inp, np.float32, [0])
     got, got8 = Hx.to_np(vel), Hx.to_np(vel8)
     cs, cs8 = Hx.cosine(got, want), Hx.cosine(got8, want)
-    print(f"step_1024: cos {cs:.6f} max_abs {Hx.max_abs(got, want):.4g}; e4m3 single-stream: cos {cs8:.6f} "
+    print(f"step_1024: cos {cs:.6f} max_abs {Hx.max_abs(got, want):.4g}; e4m3 projections: cos {cs8:.6f} "
           f"max_abs {Hx.max_abs(got8, want):.4g}")
     assert cs >= STEP_COS
     assert cs8 >= FP8_STEP_COS
@@ -311,7 +312,17 @@ def test_blocks_wider_config(dit, kind):
     run_block(dit, kind, WIDE_WL, seed=4)
 
 
-@pytest.mark.parametrize("wl", [synth.WORKLOADS["single_block_1024"], TINY_REF], ids=lambda w: w.name)
-def test_single_block_fp8(dit, wl):
-    """The single-stream block with its fused projection in e4m3 against the oracle."""
-    run_block(dit, "single", wl, seed=0, fp8=True)
+@pytest.mark.parametrize("wl,scope", [(synth.WORKLOADS["single_block_1024"], "all"), (TINY_REF, "all"),
+                                      (TINY_REF, "fused")], ids=lambda v: getattr(v, "name", v))
+def test_single_block_fp8(dit, wl, scope):
+    """The single-stream block with its projections in e4m3 (the fused QKV + MLP-in only, or
+    also the out-projection over [attn | act]) against the oracle."""
+    run_block(dit, "single", wl, seed=0, fp8=scope)
+
+
+@pytest.mark.parametrize("wl", [synth.WORKLOADS["dual_block_1024"], TINY_REF], ids=lambda w: w.name)
+def test_dual_block_fp8(dit, wl):
+    """The dual-stream block with all four projections of both streams in e4m3 (QKV and
+    MLP-in on adaLN's quantised output, out and MLP-out on the quantised attention output and
+    activations) against the oracle."""
+    run_block(dit, "dual", wl, seed=0, fp8="all")
