@@ -320,6 +320,68 @@ def final_layer(x_img, shift, scale, w_proj, cfg: Config, dtype=np.float64) -> n
 
 
 # ----------------------------------------------------------------------------------
+# e4m3 quantisation (reading R26 of the [pyref] KleinTT constructor's precision knob).
+# The pages name the knob without a format; the format here is the common 8-bit float
+# with 1 sign bit, 4 exponent bits (bias 7) and 3 mantissa bits: normal values
+# (-1)^s 2^(e-7) (1 + m/8) for e in 1..15 (e = 15, m = 7 is NaN, so the largest finite
+# value is 1.75 * 2^8 = 448), subnormals (-1)^s 2^-6 (m/8) for e = 0.
+# ----------------------------------------------------------------------------------
+E4M3_MAX = 448.0
+
+
+def e4m3_decode(code: int) -> float:
+    """The value of one e4m3 byte (NaN for the two NaN codes)."""
+    s, e, m = (code >> 7) & 1, (code >> 3) & 15, code & 7
+    if e == 15 and m == 7:
+        return float("nan")
+    mag = 2.0 ** -6 * (m / 8.0) if e == 0 else 2.0 ** (e - 7) * (1.0 + m / 8.0)
+    return -mag if s else mag
+
+
+def e4m3_encode(x: float) -> int:
+    """Round x to the nearest e4m3 value, ties to even mantissa, saturating to +-448
+    (finite inputs only).  Pure-Python: the grid is walked per binade."""
+    sign = 0x80 if (x < 0 or (x == 0 and np.signbit(x))) else 0
+    a = abs(float(x))
+    if a >= E4M3_MAX:
+        return sign | 0x7E
+    if a < 2.0 ** -6:  # subnormal binade (and zero): steps of 2^-9
+        q = _round_half_even(a / 2.0 ** -9)
+        return sign | q  # q == 8 is the smallest normal, code 0x08, by construction
+    e = int(np.floor(np.log2(a)))
+    while 2.0 ** e > a:  # guard the log2 rounding at binade edges
+        e -= 1
+    while 2.0 ** (e + 1) <= a:
+        e += 1
+    q = _round_half_even(a / 2.0 ** (e - 3))  # 8 .. 16
+    if q == 16:
+        e, q = e + 1, 8
+    code = ((e + 7) << 3) | (q - 8)
+    return sign | min(code, 0x7E)
+
+
+def _round_half_even(t: float) -> int:
+    f = int(np.floor(t))
+    r = t - f
+    if r > 0.5 or (r == 0.5 and f % 2 == 1):
+        f += 1
+    return f
+
+
+def quantize_rows_e4m3(w: np.ndarray):
+    """Per-row e4m3 quantisation as the library's weight preparation defines it, in fp32
+    arithmetic: scale = max|w[r,:]| / 448 (1 for an all-zero row), q = e4m3(w * (1/scale)).
+    Returns (codes uint8 [rows, cols], scale float32 [rows])."""
+    w = np.asarray(w, dtype=np.float32)
+    amax = np.abs(w).max(axis=1).astype(np.float32)
+    scale = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
+    inv = (np.float32(1.0) / scale).astype(np.float32)
+    scaled = (w * inv[:, None]).astype(np.float32)
+    codes = np.array([[e4m3_encode(v) for v in row] for row in scaled], dtype=np.uint8)
+    return codes, scale
+
+
+# ----------------------------------------------------------------------------------
 # The whole step and the 4-step loop
 # ----------------------------------------------------------------------------------
 @dataclass

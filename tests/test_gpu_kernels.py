@@ -175,3 +175,26 @@ def test_bounded_wait_reports_timeout_and_context_survives(dit, ws):
     st, _ = dit.dit_sync_status(ws)          # cleared by the previous read
     assert st == dit.DIT_OK
     test_attention(dit, 1, 1, 128, 1.0, ws)   # the context is still usable
+
+
+def test_quantize_rows_fp8_bit_exact(dit):
+    """dit_quantize_rows_fp8 against the oracle's e4m3 quantiser, byte for byte: fp32
+    scale = max|row| / 448, fp32 reciprocal and product, round-to-nearest-even with
+    saturation.  Rows span small, large and all-zero values; 272 columns are not a multiple
+    of the kernel's 256-thread stride."""
+    rows, cols = 37, 272
+    w = _randn((rows, cols), 0.05, seed=21)
+    w[3] = 0.0
+    w[5] *= 1.0e4
+    w[9] *= 1.0e-6
+    w[11, 7] = 3.0e4
+    wd = w.to(DEV)
+    q = torch.empty((rows, cols), dtype=torch.uint8, device=DEV)
+    sc = torch.empty((rows,), dtype=torch.float32, device=DEV)
+    dit.dit_quantize_rows_fp8(wd, rows, cols, q, sc)
+    torch.cuda.synchronize()
+    codes, scale = O.quantize_rows_e4m3(Hx.to_np(w, np.float32))
+    assert np.array_equal(sc.cpu().numpy(), scale)
+    got = q.cpu().numpy()
+    bad = np.argwhere(got != codes)
+    assert bad.size == 0, (bad[:5], got[tuple(bad[0])] if bad.size else None)

@@ -366,3 +366,42 @@ def test_klein_parameter_count_is_about_4b():
     assert abs(billions - float(STRUCT["model_params_billion"])) < 0.25, billions
     assert len(w["dual"]) == int(STRUCT["n_dual"]) and len(w["single"]) == int(STRUCT["n_single"])
     assert synth.KLEIN.txt_dim == int(STRUCT["text_dim"]) == 3 * 2560
+
+
+# ---- e4m3 quantisation (reading R26): pinned by encodings fixed by the format's definition
+def test_e4m3_known_encodings_ties_and_saturation():
+    # 1 = 2^0 (e 7, m 0); 448 = 2^8 * 1.75 (e 15, m 6); 240 = 2^7 * 1.875 (e 14, m 7);
+    # 2^-6 is the smallest normal (e 1); 2^-9 the smallest subnormal (m 1); -2 = sign | e 8
+    fixed = {1.0: 0x38, 448.0: 0x7E, 240.0: 0x77, 2.0 ** -6: 0x08, 2.0 ** -9: 0x01, -2.0: 0xC0, 0.0: 0x00,
+             0.3125: 0x2A}
+    for v, code in fixed.items():
+        assert O.e4m3_encode(v) == code, (v, hex(O.e4m3_encode(v)))
+    # ties go to the even mantissa: 1.0625 between m 0 and m 1 -> m 0; 1.1875 between m 1 and
+    # m 2 -> m 2; 2^-10 between 0 and the smallest subnormal -> 0
+    assert O.e4m3_encode(1.0625) == 0x38 and O.e4m3_encode(1.1875) == 0x3A and O.e4m3_encode(2.0 ** -10) == 0x00
+    # nearest, not truncation: 0.3 lies nearer 0.3125 (m 2) than 0.28125 (m 1)
+    assert O.e4m3_encode(0.3) == 0x2A
+    # saturation to the largest finite value instead of NaN / overflow
+    assert O.e4m3_encode(464.0) == 0x7E and O.e4m3_encode(1e9) == 0x7E and O.e4m3_encode(-1e9) == 0xFE
+
+
+def test_e4m3_codes_round_trip_and_are_monotonic():
+    finite = [c for c in range(128) if c != 0x7F]
+    vals = [O.e4m3_decode(c) for c in finite]
+    assert all(b > a for a, b in zip(vals, vals[1:]))                 # strictly increasing magnitudes
+    assert vals[-1] == 448.0 and vals[1] == 2.0 ** -9
+    for c in finite + [c | 0x80 for c in finite if c]:
+        assert O.e4m3_encode(O.e4m3_decode(c)) == c
+    assert np.isnan(O.e4m3_decode(0x7F)) and np.isnan(O.e4m3_decode(0xFF))
+
+
+def test_quantize_rows_e4m3_scales_and_zero_rows():
+    w = np.zeros((3, 16), np.float32)
+    w[0, 5] = -896.0          # max |w| = 896 -> scale 2, the element maps to -448
+    w[0, 6] = 1.0             # 1 / 2 = 0.5 -> e 6, m 0
+    w[2] = 0.25
+    codes, scale = O.quantize_rows_e4m3(w)
+    assert scale.tolist() == [2.0, 1.0, np.float32(0.25 / 448.0)]
+    assert codes[0, 5] == 0xFE and codes[0, 6] == 0x30 and codes[0, 0] == 0x00
+    assert (codes[1] == 0).all()                                      # all-zero row: scale 1, codes 0
+    assert (codes[2] == 0x7E).all()                                   # the row maximum maps to 448
