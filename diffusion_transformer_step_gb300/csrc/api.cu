@@ -19,6 +19,7 @@ namespace {
 std::atomic<unsigned long long> g_launches{0};
 std::mutex g_timing_mu;
 bool g_timing_on = false;
+unsigned int g_timing_mask = ~0u;  // classes whose launches get an event pair
 struct TimingRec {
   int cls;
   cudaEvent_t start, stop;
@@ -39,7 +40,7 @@ const char* kernel_class_name(int cls) {
 LaunchScope::LaunchScope(int cls, cudaStream_t stream) : slot_(-1), stream_(stream) {
   g_launches.fetch_add(1, std::memory_order_relaxed);
   std::lock_guard<std::mutex> lk(g_timing_mu);
-  if (g_timing_on && g_rec_used < (int)g_recs.size()) {
+  if (g_timing_on && ((g_timing_mask >> cls) & 1u) && g_rec_used < (int)g_recs.size()) {
     slot_ = g_rec_used++;
     g_recs[slot_].cls = cls;
     cudaEventRecord(g_recs[slot_].start, stream);
@@ -952,5 +953,12 @@ dit_status dit_timing_end(int* n, int* classes, float* ms, int cap) {
 }
 
 const char* dit_kernel_class_name(int cls) { return kernel_class_name(cls); }
+
+dit_status dit_timing_select(unsigned int class_mask) {
+  if (class_mask == 0u) return DIT_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_timing_mu);
+  g_timing_mask = class_mask;
+  return DIT_OK;
+}
 
 }  // extern "C"

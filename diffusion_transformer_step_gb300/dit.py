@@ -107,6 +107,7 @@ _SIGS = {
     "dit_selftest_wait_timeout": (_I, [_P, _SZ, C.c_uint, _P]),
     "dit_launch_count": (C.c_ulonglong, []),
     "dit_timing_begin": (_I, [_I]),
+    "dit_timing_select": (_I, [C.c_uint]),
     "dit_timing_end": (_I, [C.POINTER(_I), C.POINTER(_I), C.POINTER(_F), _I]),
     "dit_kernel_class_name": (C.c_char_p, [_I]),
 }
@@ -318,6 +319,10 @@ def dit_launch_count() -> int:
 
 def dit_timing_begin(max_records: int):
     _check("dit_timing_begin", lib().dit_timing_begin(max_records))
+
+
+def dit_timing_select(class_mask: int):
+    _check("dit_timing_select", lib().dit_timing_select(class_mask & 0xFFFFFFFF))
 
 
 def dit_timing_end(cap: int):

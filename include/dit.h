@@ -356,6 +356,12 @@ unsigned long long dit_launch_count(void);
  * recorded on the launch's own stream. */
 dit_status dit_timing_begin(int max_records);
 
+/* Restrict the event pairs of dit_timing_begin to launches whose class bit is set in
+ * class_mask (bit c = class c; ~0u, the initial value, records every class), so that a
+ * timed region pays for events only around the kernels it measures.  Takes effect for
+ * launches issued after the call.  Returns DIT_ERR_INVALID_ARG for a zero mask. */
+dit_status dit_timing_select(unsigned int class_mask);
+
 /* Stop recording, synchronise the recorded events and return up to `cap` records:
  * classes[i] and ms[i] (device time of launch i).  *n receives the count. */
 dit_status dit_timing_end(int* n, int* classes, float* ms, int cap);
