@@ -54,6 +54,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) adaln_kernel(AdaLNArgs a) {
   fence_mbar_init();
   __syncthreads();
   const WaitCtx wc{a.status, &abort_flag, kWaitLimitNs};
+  grid_dependency_wait();  // x and y belong to earlier kernels of the stream
+  allow_dependents();
 
   auto row_src = [&](long long row) -> const uint8_t* {
     const int b = (int)(row / a.rows);
@@ -232,6 +234,8 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_act_kernel(const bf16*
                                                                      long long src_bstride, int ld, int col0, int rows,
                                                                      int cols, uint8_t* __restrict__ dst,
                                                                      float* __restrict__ scale) {
+  grid_dependency_wait();  // src and dst belong to earlier kernels of the stream
+  allow_dependents();
   const long long row = blockIdx.x;  // batch * rows
   const int b = (int)(row / rows);
   const int r = (int)(row - (long long)b * rows);
@@ -302,8 +306,7 @@ cudaError_t launch_kind(const AdaLNArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
   }
   LaunchScope scope(kClsAdaLN, s);
-  k<<<(unsigned)grid, warps * 32, smem, s>>>(a);
-  return cudaGetLastError();
+  return launch_k(k, dim3((unsigned)grid), dim3(warps * 32), smem, s, a);
 }
 
 template <int VPL>
@@ -360,8 +363,7 @@ cudaError_t launch_quantize_act(const bf16* src, long long src_bstride, int ld, 
   if ((long long)batch * rows == 0) return cudaSuccess;
   if (!quantize_act_supports(cols)) return cudaErrorInvalidValue;
   LaunchScope scope(kClsQuantAct, s);
-  quantize_act_kernel<<<(unsigned)((long long)batch * rows), kQuantThreads, 0, s>>>(src, src_bstride, ld, col0, rows,
-                                                                                    cols, dst, scale);
-  return cudaGetLastError();
+  return launch_k(quantize_act_kernel, dim3((unsigned)((long long)batch * rows)), dim3(kQuantThreads), 0, s, src,
+                  src_bstride, ld, col0, rows, cols, dst, scale);
 }
 }  // namespace dit

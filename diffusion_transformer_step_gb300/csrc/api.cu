@@ -2,6 +2,7 @@
 // sequence of a dual-stream block, a single-stream block and the whole step, and the
 // host runtime pieces (launch accounting, per-launch timing, TMA descriptor encoding).
 #include <atomic>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -49,6 +50,14 @@ LaunchScope::LaunchScope(int cls, cudaStream_t stream) : slot_(-1), stream_(stre
 
 LaunchScope::~LaunchScope() {
   if (slot_ >= 0) cudaEventRecord(g_recs[slot_].stop, stream_);
+}
+
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* e = getenv("DIT_NO_PDL");
+    return !(e && e[0] == '1');
+  }();
+  return on;
 }
 
 int sm_count() {

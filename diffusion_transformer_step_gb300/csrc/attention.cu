@@ -274,6 +274,8 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtx wc{P.status, abort_flag, kWaitLimitNs};
+  grid_dependency_wait();  // Q, K, V and the output belong to earlier kernels of the stream
+  allow_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -488,8 +490,7 @@ cudaError_t launch_attention(int batch, int heads, int n, const bf16* q, const b
   }
   dim3 grid((n + 2 * kBQ - 1) / (2 * kBQ), heads, batch);
   LaunchScope scope(kClsAttention, s);
-  attention_kernel<<<grid, kThreads, kSmemBytes, s>>>(P);
-  return cudaGetLastError();
+  return launch_k(attention_kernel, grid, dim3(kThreads), kSmemBytes, s, P);
 }
 
 }  // namespace dit

@@ -302,6 +302,15 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream serialisation
+// may start while its predecessor on the stream still runs.  grid_dependency_wait() blocks
+// until every prerequisite grid has completed and its memory is visible; nothing before it
+// may read or write memory that an earlier kernel writes or reads.  allow_dependents()
+// lets the next kernel on the stream start launching (it still waits in its own
+// grid_dependency_wait()).  Both are no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
 
 __device__ __forceinline__ bool elect_one() { return (threadIdx.x & 31u) == 0u; }

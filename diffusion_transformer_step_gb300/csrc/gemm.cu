@@ -374,6 +374,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtx wc{P.status, abort_flag, kWaitLimitNs};
+  grid_dependency_wait();  // A, residuals and outputs belong to earlier kernels of the stream
+  allow_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (both CTAs)
@@ -677,11 +679,8 @@ cudaError_t launch_gemm(const GemmProblemHost* probs, int nprob, int batch, floa
   const int pairs_max = sm_count() / 2;
   const int pairs = tiles < pairs_max ? tiles : pairs_max;
   LaunchScope scope(cls, s);
-  if (fp8)
-    gemm_kernel<true><<<2 * pairs, kThreads, kSmemBytes, s>>>(P);
-  else
-    gemm_kernel<false><<<2 * pairs, kThreads, kSmemBytes, s>>>(P);
-  return cudaGetLastError();
+  if (fp8) return launch_k(gemm_kernel<true>, dim3(2 * pairs), dim3(kThreads), kSmemBytes, s, P);
+  return launch_k(gemm_kernel<false>, dim3(2 * pairs), dim3(kThreads), kSmemBytes, s, P);
 }
 
 }  // namespace dit

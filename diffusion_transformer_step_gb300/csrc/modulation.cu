@@ -18,6 +18,8 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const bf16* __restric
                                                             float* __restrict__ y_f32, bf16* __restrict__ y_bf16,
                                                             int y_stride) {
   extern __shared__ float xs[];  // [NB][k]
+  grid_dependency_wait();
+  allow_dependents();
   for (int i = threadIdx.x; i < NB * k; i += blockDim.x) xs[i] = x[i];
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -66,6 +68,8 @@ __global__ void __launch_bounds__(kWarps * 32) timestep_in_kernel(const bf16* __
                                                                    int time_dim, const float* __restrict__ sigma,
                                                                    int batch, float* __restrict__ h) {
   extern __shared__ float sv[];  // [batch][time_dim]
+  grid_dependency_wait();
+  allow_dependents();
   const int half = time_dim / 2;
   for (int i = threadIdx.x; i < batch * half; i += blockDim.x) {
     const int b = i / half, kk = i - b * half;
@@ -96,6 +100,8 @@ struct SigmaList {
 
 __global__ void denoise_setup_kernel(SigmaList sl, int steps, int batch, float* __restrict__ sigma,
                                      float* __restrict__ coef) {
+  grid_dependency_wait();
+  allow_dependents();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= steps * batch) return;
   const int k = i / batch;
@@ -115,8 +121,7 @@ cudaError_t gemv_nb(const bf16* W, int n, int k, const float* x, int act, float*
   const int cap = sm_count() * 8;
   if (grid > cap) grid = cap;
   LaunchScope scope(kClsModulation, s);
-  gemv_kernel<NB><<<grid, kWarps * 32, smem, s>>>(W, n, k, x, act, y_f32, y_bf16, y_stride);
-  return cudaGetLastError();
+  return launch_k(gemv_kernel<NB>, dim3(grid), dim3(kWarps * 32), smem, s, W, n, k, x, act, y_f32, y_bf16, y_stride);
 }
 
 }  // namespace
@@ -151,8 +156,7 @@ cudaError_t launch_denoise_setup(const float* sigmas_host, int steps, int batch,
   for (int k = 0; k <= steps; ++k) sl.v[k] = sigmas_host[k];
   const int n = steps * batch;
   LaunchScope scope(kClsModulation, s);
-  denoise_setup_kernel<<<(n + 127) / 128, 128, 0, s>>>(sl, steps, batch, sigma, coef);
-  return cudaGetLastError();
+  return launch_k(denoise_setup_kernel, dim3((n + 127) / 128), dim3(128), 0, s, sl, steps, batch, sigma, coef);
 }
 
 cudaError_t launch_timestep_in(const bf16* t_in, int H, int time_dim, const float* sigma, int batch, float* h,
@@ -166,8 +170,7 @@ cudaError_t launch_timestep_in(const bf16* t_in, int H, int time_dim, const floa
   const int cap = sm_count() * 4;
   if (grid > cap) grid = cap;
   LaunchScope scope(kClsModulation, s);
-  timestep_in_kernel<<<grid, kWarps * 32, smem, s>>>(t_in, H, time_dim, sigma, batch, h);
-  return cudaGetLastError();
+  return launch_k(timestep_in_kernel, dim3(grid), dim3(kWarps * 32), smem, s, t_in, H, time_dim, sigma, batch, h);
 }
 
 }  // namespace dit

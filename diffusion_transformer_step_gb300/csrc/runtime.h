@@ -46,6 +46,25 @@ class LaunchScope {
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
+// Launch a step kernel with programmatic stream serialisation (its prologue may overlap the
+// previous kernel's tail; the kernel itself calls grid_dependency_wait() before touching
+// dependent memory).  DIT_NO_PDL=1 in the environment turns the attribute off.
+bool pdl_enabled();
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Encode a bf16 tiled TMA descriptor with 128-byte swizzle.  dims/strides innermost
 // first; strides are in bytes for dims 1..rank-1.  Returns false on failure.
 bool encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
