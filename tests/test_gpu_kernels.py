@@ -163,6 +163,26 @@ def test_attention(dit, batch, heads, n, qscale, ws):
     assert (out[..., heads * 128:] == 0).all()
 
 
+def test_attention_at_the_sequence_limit(dit, ws):
+    """Attention at the library's token limit (2^20 tokens less a ragged 13): 8192 key
+    blocks through the two-slot ring and 4096 CTAs.  Sampled query rows (first tiles, the
+    middle, the last full tile and the ragged tail) against the oracle over every key, in
+    fp32 for this size."""
+    n = (1 << 20) - 13
+    q = _randn((1, 1, n, 128), 1.0, seed=31)
+    k = _randn((1, 1, n, 128), 1.0, seed=32)
+    v = _randn((1, 1, n, 128), 1.0, seed=33)
+    out = torch.zeros((1, n, 128), dtype=torch.bfloat16, device=DEV)
+    dit.dit_attention(1, 1, n, q.to(DEV), k.to(DEV), v.to(DEV), out, 128, ws, ws.numel())
+    _check_status(dit, ws)
+    rows = [0, 1, 127, 128, 255, 256, n // 2, n // 2 + 129, n - 300, n - 141, n - 129, n - 13, n - 1]
+    qs = Hx.to_np(q[0, 0, rows], np.float32)[None, :, None, :]
+    kk = Hx.to_np(k[0, 0], np.float32)[None, :, None, :]
+    vv = Hx.to_np(v[0, 0], np.float32)[None, :, None, :]
+    want = O.attention(qs, kk, vv)[0, :, 0, :]
+    _cmp(out[0, rows], want, atol=3e-2, cos_min=0.999)
+
+
 def test_bounded_wait_reports_timeout_and_context_survives(dit, ws):
     """A device wait that can never complete gives up after its limit: the status word
     reports DIT_ERR_TIMEOUT with the waiting site, and later work on the GPU still runs."""
