@@ -18,7 +18,7 @@ namespace dit {
 namespace {
 
 constexpr uint32_t kSiteAdaLN = 0x301;
-constexpr int kMaxWarps = 8;
+constexpr int kMaxWarps = 16;
 constexpr size_t kSmemBudget = 200 * 1024;
 
 __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -28,8 +28,32 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
                : "memory");
 }
 
+// Element k * 256 + 8 * lane + j (j < 8) of the staged row, as fp32 pairs.
+template <bool F32IN>
+__device__ __forceinline__ void load8(const uint8_t* buf, int k, int lane, float2 (&x)[4]) {
+  if (F32IN) {
+    const float4* xf = reinterpret_cast<const float4*>(buf) + 2 * (k * 32 + lane);
+    const float4 f0 = xf[0], f1 = xf[1];
+    x[0] = make_float2(f0.x, f0.y);
+    x[1] = make_float2(f0.z, f0.w);
+    x[2] = make_float2(f1.x, f1.y);
+    x[3] = make_float2(f1.z, f1.w);
+  } else {
+    const uint4 u = reinterpret_cast<const uint4*>(buf)[k * 32 + lane];
+    x[0] = unpack_bf16x2(u.x);
+    x[1] = unpack_bf16x2(u.y);
+    x[2] = unpack_bf16x2(u.z);
+    x[3] = unpack_bf16x2(u.w);
+  }
+}
+
 // kFp8Out: y is written as e4m3 with one fp32 scale per row (y ~ scale * q, scale =
 // max|y| / 448, the largest finite e4m3), the A operand of an fp8 projection.
+// The row stays in shared memory and is read once per pass: pass 1 the shifted sums
+// (sum and sum of squares of x - x[0], exact enough in fp32 for any mean: the shift is a
+// value of the row), pass 2 the modulated output (and, for e4m3, pass 2 the row maximum of
+// y and pass 3 the codes).  Holding nothing of the row in registers lets 16 warps share an
+// SM.  Packed fp32x2 arithmetic throughout.
 template <int VPL, bool F32IN, bool kFp8Out>  // 8-element vectors per lane: hidden = VPL * 256
 __global__ void __launch_bounds__(kMaxWarps * 32, 1) adaln_kernel(AdaLNArgs a) {
   constexpr int H = VPL * 256;
@@ -85,31 +109,97 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) adaln_kernel(AdaLNArgs a) {
     const int b = (int)(r / a.rows);
     const int rw = (int)(r - (long long)b * a.rows);
 
-    float v[VPL][8];
-    float sum = 0.f;
-#pragma unroll
+    // pass 1: shifted sums
+    const float shift0 = F32IN ? reinterpret_cast<const float*>(buf)[0]
+                               : __bfloat162float(reinterpret_cast<const bf16*>(buf)[0]);
+    const float2 nk = make_float2(-shift0, -shift0);
+    float2 s1 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
+#pragma unroll 4
     for (int k = 0; k < VPL; ++k) {
-      if (F32IN) {
-        const float4* xf = reinterpret_cast<const float4*>(buf);
-        const float4 f0 = xf[2 * (k * 32 + lane)], f1 = xf[2 * (k * 32 + lane) + 1];
-        v[k][0] = f0.x; v[k][1] = f0.y; v[k][2] = f0.z; v[k][3] = f0.w;
-        v[k][4] = f1.x; v[k][5] = f1.y; v[k][6] = f1.z; v[k][7] = f1.w;
-      } else {
-        const uint4 u = reinterpret_cast<const uint4*>(buf)[k * 32 + lane];
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+      float2 x[4];
+      load8<F32IN>(buf, k, lane, x);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float2 f = unpack_bf16x2(w[j]);
-          v[k][2 * j] = f.x;
-          v[k][2 * j + 1] = f.y;
-        }
+      for (int j = 0; j < 4; ++j) {
+        const float2 d = __fadd2_rn(x[j], nk);
+        s1 = __fadd2_rn(s1, d);
+        s2 = __ffma2_rn(d, d, s2);
+      }
+    }
+    float sum = s1.x + s1.y, sq = s2.x + s2.y;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      sq += __shfl_xor_sync(0xffffffffu, sq, o);
+    }
+    const float dm = sum * (1.0f / H);  // mean - shift0
+    const float var = fmaxf(sq * (1.0f / H) - dm * dm, 0.f);
+    const float rstd = rsqrtf(var + a.eps);
+    const float mean = shift0 + dm;
+    // n = x * rstd - mean * rstd
+    const float2 rs2 = make_float2(rstd, rstd), mb2 = make_float2(-mean * rstd, -mean * rstd);
+    const float2 one = make_float2(1.f, 1.f);
+
+    const bool lo = rw < a.split;
+    const uint4* shv = reinterpret_cast<const uint4*>((lo ? a.shift_lo : a.shift_hi) + b * a.mod_stride);
+    const uint4* scv = reinterpret_cast<const uint4*>((lo ? a.scale_lo : a.scale_hi) + b * a.mod_stride);
+    // y for the 8 elements of vector k of this lane
+    auto modulated = [&](int k, float2 (&y)[4]) {
+      float2 x[4];
+      load8<F32IN>(buf, k, lane, x);
+      const uint4 sh = __ldg(shv + k * 32 + lane);
+      const uint4 sc = __ldg(scv + k * 32 + lane);
+      const uint32_t shw[4] = {sh.x, sh.y, sh.z, sh.w};
+      const uint32_t scw[4] = {sc.x, sc.y, sc.z, sc.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 n = __ffma2_rn(x[j], rs2, mb2);
+        y[j] = __ffma2_rn(__fadd2_rn(unpack_bf16x2(scw[j]), one), n, unpack_bf16x2(shw[j]));
+      }
+    };
+
+    if (!kFp8Out) {
+      uint4* yv = reinterpret_cast<uint4*>(a.y + b * a.y_bstride + (long long)rw * H);
+#pragma unroll 4
+      for (int k = 0; k < VPL; ++k) {
+        float2 y[4];
+        modulated(k, y);
+        yv[k * 32 + lane] = make_uint4(pack_bf16x2(y[0].x, y[0].y), pack_bf16x2(y[1].x, y[1].y),
+                                       pack_bf16x2(y[2].x, y[2].y), pack_bf16x2(y[3].x, y[3].y));
+      }
+    } else {
+      float amax = 0.f;
+#pragma unroll 4
+      for (int k = 0; k < VPL; ++k) {
+        float2 y[4];
+        modulated(k, y);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) amax = fmaxf(amax, fmaxf(fabsf(y[j].x), fabsf(y[j].y)));
       }
 #pragma unroll
-      for (int j = 0; j < 8; ++j) sum += v[k][j];
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      const float scale = amax > 0.f ? amax / 448.0f : 1.0f;
+      const float inv = 1.0f / scale;
+      uint2* qv = reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(a.y_q) + b * a.y_bstride + (long long)rw * H);
+#pragma unroll 4
+      for (int k = 0; k < VPL; ++k) {
+        float2 y[4];
+        modulated(k, y);
+        uint32_t w[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const __nv_fp8x2_storage_t q0 =
+              __nv_cvt_float2_to_fp8x2(make_float2(y[2 * h].x * inv, y[2 * h].y * inv), __NV_SATFINITE, __NV_E4M3);
+          const __nv_fp8x2_storage_t q1 = __nv_cvt_float2_to_fp8x2(
+              make_float2(y[2 * h + 1].x * inv, y[2 * h + 1].y * inv), __NV_SATFINITE, __NV_E4M3);
+          w[h] = (uint32_t)q0 | ((uint32_t)q1 << 16);
+        }
+        qv[k * 32 + lane] = make_uint2(w[0], w[1]);
+      }
+      if (lane == 0) a.y_scale[(long long)b * a.rows + rw] = scale;
     }
     ++consumed;
-    // Every lane has its part of the row in registers: the stage may be refilled (the
-    // generic-proxy reads are ordered before the bulk copy's async-proxy writes).
+    // every lane has finished reading the staged row: the stage may be refilled (the
+    // generic-proxy reads are ordered before the bulk copy's async-proxy writes)
     __syncwarp();
     if (lane == 0) {
       fence_proxy_async_smem();
@@ -119,73 +209,6 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) adaln_kernel(AdaLNArgs a) {
         bulk_copy_g2s(st ? buf1 : buf0, row_src(nrow), kRowBytes, &bar[st]);
         ++issued;
       }
-    }
-
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    const float mean = sum * (1.0f / H);
-    float sq = 0.f;
-#pragma unroll
-    for (int k = 0; k < VPL; ++k)
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float d = v[k][j] - mean;
-        sq += d * d;
-      }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
-    const float rstd = rsqrtf(sq * (1.0f / H) + a.eps);
-
-    const bool lo = rw < a.split;
-    const uint4* shv = reinterpret_cast<const uint4*>((lo ? a.shift_lo : a.shift_hi) + b * a.mod_stride);
-    const uint4* scv = reinterpret_cast<const uint4*>((lo ? a.scale_lo : a.scale_hi) + b * a.mod_stride);
-    float amax = 0.f;
-#pragma unroll
-    for (int k = 0; k < VPL; ++k) {
-      const uint4 sh = __ldg(shv + k * 32 + lane);
-      const uint4 sc = __ldg(scv + k * 32 + lane);
-      const uint32_t shw[4] = {sh.x, sh.y, sh.z, sh.w};
-      const uint32_t scw[4] = {sc.x, sc.y, sc.z, sc.w};
-      uint32_t o[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float2 s2 = unpack_bf16x2(shw[j]);
-        const float2 c2 = unpack_bf16x2(scw[j]);
-        const float y0 = (1.0f + c2.x) * ((v[k][2 * j] - mean) * rstd) + s2.x;
-        const float y1 = (1.0f + c2.y) * ((v[k][2 * j + 1] - mean) * rstd) + s2.y;
-        if (kFp8Out) {
-          v[k][2 * j] = y0;
-          v[k][2 * j + 1] = y1;
-          amax = fmaxf(amax, fmaxf(fabsf(y0), fabsf(y1)));
-        } else {
-          o[j] = pack_bf16x2(y0, y1);
-        }
-      }
-      if (!kFp8Out) {
-        uint4* yv = reinterpret_cast<uint4*>(a.y + b * a.y_bstride + (long long)rw * H);
-        yv[k * 32 + lane] = make_uint4(o[0], o[1], o[2], o[3]);
-      }
-    }
-    if (kFp8Out) {
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-      const float scale = amax > 0.f ? amax / 448.0f : 1.0f;
-      const float inv = 1.0f / scale;
-      uint2* qv = reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(a.y_q) + b * a.y_bstride + (long long)rw * H);
-#pragma unroll
-      for (int k = 0; k < VPL; ++k) {
-        uint32_t w[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const __nv_fp8x2_storage_t q0 =
-              __nv_cvt_float2_to_fp8x2(make_float2(v[k][4 * h] * inv, v[k][4 * h + 1] * inv), __NV_SATFINITE, __NV_E4M3);
-          const __nv_fp8x2_storage_t q1 = __nv_cvt_float2_to_fp8x2(
-              make_float2(v[k][4 * h + 2] * inv, v[k][4 * h + 3] * inv), __NV_SATFINITE, __NV_E4M3);
-          w[h] = (uint32_t)q0 | ((uint32_t)q1 << 16);
-        }
-        qv[k * 32 + lane] = make_uint2(w[0], w[1]);
-      }
-      if (lane == 0) a.y_scale[(long long)b * a.rows + rw] = scale;
     }
   }
   // After an early exit, let this warp's copies still in flight land (bounded) before the
