@@ -202,12 +202,14 @@ def test_step_batch_invariance_ref_b4(dit):
 
 
 @pytest.mark.parametrize("host_io", [False, True])
-def test_step_graph_replay_matches_direct_call(dit, host_io):
+@pytest.mark.parametrize("fp8", [False, "all"], ids=["bf16", "e4m3"])
+def test_step_graph_replay_matches_direct_call(dit, host_io, fp8):
     """A captured step replays to the same bits as the direct call, also after the inputs
-    change between replays (the graph reads the buffers, not a snapshot)."""
+    change between replays (the graph reads the buffers, not a snapshot); in bf16 and with
+    every block projection in e4m3."""
     wl = TINY_REF
     logical = synth.model_weights(wl.widths, seed=6)
-    W = dit.DeviceWeights(wl.widths, logical)
+    W = dit.DeviceWeights(wl.widths, logical, fp8=fp8)
     shape, rope, ws, nbytes = _setup(dit, wl, W)
     a, b = synth.step_inputs(wl, seed=6), synth.step_inputs(wl, seed=7)
     loc = "cpu" if host_io else DEV
@@ -228,9 +230,12 @@ def test_step_graph_replay_matches_direct_call(dit, host_io):
             dit.dit_graph_launch(g)
             _status(dit, ws)
             # every kernel of the step is counted: modulation 3, embedders 1 (+1 with
-            # references), 7 per dual block, 4 per single block, final layer 2
+            # references), 7 per dual block, 4 per single block, final layer 2; e4m3 adds
+            # the quantising pass before each out-projection (2 per dual, 1 per single block)
             wd = wl.widths
             want_kernels = 3 + 1 + (1 if wl.n_ref else 0) + 7 * wd.n_dual + 4 * wd.n_single + 2
+            if fp8:
+                want_kernels += 2 * wd.n_dual + wd.n_single
             assert dit.dit_launch_count() - before == want_kernels
             want, _ = _step(dit, wl, logical, inp, W)
             assert torch.equal(out.to(DEV), want)
