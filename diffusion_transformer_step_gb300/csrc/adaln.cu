@@ -4,11 +4,11 @@
 // intermediate residual stream.  HBM-bound: each row is read once (2H or 4H bytes) and
 // written once (2H bytes, or H bytes + a scale in e4m3); the modulation vectors stay in L1.
 //
-// Persistent streaming: one CTA per SM slot, one warp per row at a time.  Each warp owns a
+// Persistent streaming: one CTA per SM, one warp per row at a time.  Each warp owns a
 // two-stage shared-memory ring: its lane 0 copies whole rows in with 1-D bulk copies
 // (cp.async.bulk, completing on the stage's mbarrier), so the next row is in flight while
-// the current one is reduced (two-pass mean / variance with warp shuffles, the row in
-// registers), modulated and stored with 16-byte stores.
+// the current one is reduced from shared memory (shifted sums with warp shuffles), then
+// modulated and stored with 16-byte stores.
 #include <cuda_fp8.h>
 
 #include "runtime.h"
@@ -317,8 +317,8 @@ cudaError_t launch_kind(const AdaLNArgs& a, cudaStream_t s) {
   int warps = (int)(kSmemBudget / (2 * row_bytes));
   if (warps > kMaxWarps) warps = kMaxWarps;
   const size_t smem = (size_t)warps * 2 * row_bytes;
-  // One CTA per SM (the row in registers leaves room for one 256-thread CTA): 8 warps x 2
-  // rows in flight per SM cover the HBM latency.
+  // One CTA per SM with as many warps as two staged rows each allow in the shared-memory
+  // budget (16 for bf16 rows of 3072, 8 for fp32 ones): up to 32 rows in flight per SM.
   const long long total = (long long)a.batch * a.rows;
   long long grid = (total + warps - 1) / warps;
   const long long cap = (long long)sm_count();
