@@ -12,9 +12,12 @@ tokens, batch 1).  Prints ONE JSON line on rank 0.
   e2e        the same metric through dit_step_host (replayed from a CUDA graph): pinned host
              inputs copied in and the velocity copied out inside the timed region, the host
              waiting for every step's velocity
-  roofline   the dominant kernel class (most device time in the timed region): its
-             algorithmic FLOPs per launch / its mean launch time, measured live with CUDA
-             events recorded around each launch on its own stream
+  roofline   the dominant kernel class (most device time in an untimed two-step pass that
+             records CUDA events around every launch and also gives the per-class `kernels`
+             breakdown): its algorithmic FLOPs per launch / its mean launch time, measured
+             live in the timed region with CUDA events recorded around that class's launches
+             only, on their own stream
+  fp8_variant  the same step with every block projection in e4m3 (not the headline)
   cpu_baseline  the CPU oracle (fp32 numpy) timed on a bounded sample (one dual-stream and
              one single-stream block at the same shape), scaled to the 5 + 20 blocks
   --impl reference  times the CPU oracle as the reference arm (rank 0 only).
