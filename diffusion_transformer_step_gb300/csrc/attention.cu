@@ -32,6 +32,9 @@
 // dense scalar FMA), while packed fp32x2 FMA/add, MUFU ex2 and bf16x2 conversion do not.
 // The MMA thread issues from descriptors computed once, and waiting warps sleep on the
 // barrier instead of spinning, for the same reason.
+// Output: each tile's O / l is staged as bf16 in that tile's (then free) Q shared memory, in
+// the 128-byte-swizzled layout the Q loads used, and written by TMA stores through a 3-D
+// view of the output, which clips the rows of a partial last tile.
 // Ordering: MMAs issued by one thread execute in order and a commit tracks every earlier
 // MMA of that thread, so "S_t of block j+1 is ready" also means "P_t V_j is complete":
 // the softmax may then rescale O_t and overwrite P_t without a further wait.
@@ -59,6 +62,7 @@ constexpr float kPsumLimit = 4096.0f;  // row sum of P that sends a key block do
 
 struct alignas(64) AttnParams {
   CUtensorMap q_map, k_map, v_map;
+  CUtensorMap o_map;  // output [B][n][ld_out] viewed 3-D, stored by TMA from the Q tiles' smem
   bf16* out;
   int ld_out, n, heads;
   float scale_log2;
@@ -129,7 +133,20 @@ __device__ __forceinline__ void softmax_row(uint32_t tS, int kv_valid, float c, 
   psum = ps0 + ps1;
 }
 
-enum : uint32_t { kSiteQ = 0x201, kSiteFree, kSiteReady, kSitePFull, kSiteSFull, kSiteODone };
+enum : uint32_t { kSiteQ = 0x201, kSiteFree, kSiteReady, kSitePFull, kSiteSFull, kSiteODone, kSiteOSync };
+
+// Store a {64, 128, 1} box of the output from shared memory (128-byte swizzle, the layout
+// of a Q half-tile); rows past the tensor's end are not written.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, const void* src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+__device__ __forceinline__ void tma_store_commit_and_drain() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // smem read out: safe to exit
+}
 
 
 // Shared-memory descriptors of every MMA operand, computed once: Q_t (A of S_t = Q_t K^T),
@@ -210,7 +227,7 @@ __device__ __forceinline__ void issue_pv(const Descs& d, uint32_t tmem, int t, b
 template <int ST>
 __device__ __forceinline__ bool mma_block(const Descs& d, uint32_t tmem, int j, int nkv, uint32_t idesc_qk,
                                           uint32_t idesc_pv, uint64_t* ready, uint64_t* s_full, uint64_t* p_full,
-                                          const WaitCtx& wc) {
+                                          uint64_t* o_done, const WaitCtx& wc) {
   constexpr int NST = ST ^ 1;
   const bool more = j + 1 < nkv;
   if (!mbar_wait(&ready[ST], (uint32_t)(j >> 1) & 1u, wc, kSiteReady) ||
@@ -218,11 +235,17 @@ __device__ __forceinline__ bool mma_block(const Descs& d, uint32_t tmem, int j, 
     return false;
   tc_fence_after();
   issue_pv<ST>(d, tmem, 0, j > 0, idesc_pv);
-  if (more) issue_qk<NST>(d, tmem, 0, idesc_qk, &s_full[0]);
+  if (more)
+    issue_qk<NST>(d, tmem, 0, idesc_qk, &s_full[0]);
+  else
+    umma_commit(&o_done[0]);  // tile 0's output may be read while tile 1 finishes
   if (!mbar_wait(&p_full[1], (uint32_t)j & 1u, wc, kSitePFull)) return false;
   tc_fence_after();
   issue_pv<ST>(d, tmem, 1, j > 0, idesc_pv);
-  if (more) issue_qk<NST>(d, tmem, 1, idesc_qk, &s_full[1]);
+  if (more)
+    issue_qk<NST>(d, tmem, 1, idesc_qk, &s_full[1]);
+  else
+    umma_commit(&o_done[1]);
   return true;
 }
 
@@ -235,9 +258,10 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
   uint64_t* slot_free = bars + 3;  // [2] ring slot: every MMA reading V_j and K_{j+1} done
   uint64_t* s_full = bars + 5;   // [2] per tile
   uint64_t* p_full = bars + 7;   // [2] per tile
-  uint64_t* o_done = bars + 9;
-  uint64_t* drain = bars + 10;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+  uint64_t* o_done = bars + 9;   // [2] per tile: its last PV MMA is done
+  uint64_t* drain = bars + 11;
+  uint64_t* osync = bars + 12;   // [2] per tile: its 4 warps have staged the output
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -255,7 +279,10 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 4);
     }
-    mbar_init(o_done, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&o_done[i], 1);
+      mbar_init(&osync[i], 4);
+    }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -264,6 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
     tma_prefetch_desc(&P.q_map);
     tma_prefetch_desc(&P.k_map);
     tma_prefetch_desc(&P.v_map);
+    tma_prefetch_desc(&P.o_map);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -333,10 +361,10 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
         issue_qk<0>(d, tmem, 1, idesc_qk, &s_full[1]);
       }
       for (int j = 0; j < nkv && ok; j += 2) {
-        ok = mma_block<0>(d, tmem, j, nkv, idesc_qk, idesc_pv, ready, s_full, p_full, wc);
-        if (ok && j + 1 < nkv) ok = mma_block<1>(d, tmem, j + 1, nkv, idesc_qk, idesc_pv, ready, s_full, p_full, wc);
+        ok = mma_block<0>(d, tmem, j, nkv, idesc_qk, idesc_pv, ready, s_full, p_full, o_done, wc);
+        if (ok && j + 1 < nkv)
+          ok = mma_block<1>(d, tmem, j + 1, nkv, idesc_qk, idesc_pv, ready, s_full, p_full, o_done, wc);
       }
-      umma_commit(o_done);
       umma_commit(drain);
       const uint64_t t0 = global_timer_ns();
       while (!mbar_try(drain, 0) && global_timer_ns() - t0 < 1000000000ull) {
@@ -426,26 +454,39 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
       if (lane == 0) mbar_arrive(&p_full[tile]);
     }
     if (ok) {
-      bool ok2 = mbar_wait_sleep(o_done, 0, wc, kSiteODone);
+      // Output: O_t / l, rounded to bf16, staged in Q_t's shared memory (free once the last
+      // QK is done, which precedes the last PV) in the 128-byte-swizzled layout Q was loaded
+      // in, then written by two TMA stores (one per 64-column half; rows past n clipped).
+      bool ok2 = mbar_wait_sleep(&o_done[tile], 0, wc, kSiteODone);
       ok2 = __all_sync(0xffffffffu, ok2);
       if (ok2) {
         tc_fence_after();
-        const int tok = q0 + tile * kBQ + row;
         const float inv_l = 1.0f / l_run;
-        bf16* dst = P.out + ((long long)b * n + tok) * P.ld_out + head * 128;
+        uint8_t* stage = smem + kOffQ + tile * kTileBytes;
 #pragma unroll 1
         for (int cc = 0; cc < 4; ++cc) {
           uint32_t r[32];
           tmem_load32(tO + cc * 32, r);
-          if (tok < n) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + cc * 32);
+          uint8_t* rowp = stage + (cc >> 1) * kHalfBytes + row * 128;
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              d4[i] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * i + 0]) * inv_l, __uint_as_float(r[8 * i + 1]) * inv_l),
-                                 pack_bf16x2(__uint_as_float(r[8 * i + 2]) * inv_l, __uint_as_float(r[8 * i + 3]) * inv_l),
-                                 pack_bf16x2(__uint_as_float(r[8 * i + 4]) * inv_l, __uint_as_float(r[8 * i + 5]) * inv_l),
-                                 pack_bf16x2(__uint_as_float(r[8 * i + 6]) * inv_l, __uint_as_float(r[8 * i + 7]) * inv_l));
+          for (int i = 0; i < 4; ++i) {
+            const int chunk = (cc & 1) * 4 + i;  // 16-byte chunk of the 128-byte half-row
+            *reinterpret_cast<uint4*>(rowp + ((chunk ^ (row & 7)) << 4)) =
+                make_uint4(pack_bf16x2(__uint_as_float(r[8 * i + 0]) * inv_l, __uint_as_float(r[8 * i + 1]) * inv_l),
+                           pack_bf16x2(__uint_as_float(r[8 * i + 2]) * inv_l, __uint_as_float(r[8 * i + 3]) * inv_l),
+                           pack_bf16x2(__uint_as_float(r[8 * i + 4]) * inv_l, __uint_as_float(r[8 * i + 5]) * inv_l),
+                           pack_bf16x2(__uint_as_float(r[8 * i + 6]) * inv_l, __uint_as_float(r[8 * i + 7]) * inv_l));
           }
+        }
+        fence_proxy_async_smem();  // the staged rows are visible to the TMA unit
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&osync[tile]);
+        bool ok3 = mbar_wait(&osync[tile], 0, wc, kSiteOSync);
+        ok3 = __all_sync(0xffffffffu, ok3);
+        if (ok3 && qq == 2 && lane == 0) {  // the tile's first warp (2 or 6)
+          for (int h = 0; h < 2; ++h)
+            tma_store_3d(&P.o_map, stage + h * kHalfBytes, head * 128 + h * 64, q0 + tile * kBQ, b);
+          tma_store_commit_and_drain();
         }
       }
     }
@@ -474,6 +515,9 @@ cudaError_t launch_attention(int batch, int heads, int n, const bf16* q, const b
   if (!encode_tmap_bf16(&P.q_map, q, 3, dims, str, box)) return cudaErrorInvalidValue;
   if (!encode_tmap_bf16(&P.k_map, k, 3, dims, str, box)) return cudaErrorInvalidValue;
   if (!encode_tmap_bf16(&P.v_map, v, 3, dims, str, box)) return cudaErrorInvalidValue;
+  const uint64_t odims[3] = {(uint64_t)ld_out, (uint64_t)n, (uint64_t)batch};
+  const uint64_t ostr[2] = {(uint64_t)ld_out * 2, (uint64_t)n * ld_out * 2};
+  if (!encode_tmap_bf16(&P.o_map, out, 3, odims, ostr, box)) return cudaErrorInvalidValue;
   P.out = out;
   P.ld_out = ld_out;
   P.n = n;
