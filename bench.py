@@ -424,7 +424,8 @@ def run_ours(args, wl, rank, world, local_rank):
     tr = NCU_TRAFFIC.get(dom)
     roofline = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4), "peak_source": f"bf16 sustained, of {src}",
-                "traffic": tr, "flops_per_launch": flops_cls[dom], "launch_ms_mean": round(mean_ms, 4)}
+                "traffic": tr, "flops_per_launch": flops_cls[dom], "launch_ms_mean": round(mean_ms, 4),
+                "frac_of_nominal_2250": round(achieved / 2250.0, 4)}
     flops = step_flops(wd, wl.batch, wl.n_txt, wl.n_img, wl.n_ref)
     tflops = flops / (ms_step / 1e3) / 1e12
 
