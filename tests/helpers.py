@@ -65,3 +65,46 @@ def read_rows(path):
         if line:
             rows.append([int(x) for x in line.split()])
     return np.asarray(rows, dtype=np.int64)
+
+
+def read_step_golden(path):
+    """Parse a step golden: `key = value` lines and `v <row> <token> <values...>` lines."""
+    kv, vel = {}, {}
+    for line in open(path):
+        line = line.split("#", 1)[0].strip()
+        if not line:
+            continue
+        if line.startswith("v "):
+            parts = line.split()
+            vel[(int(parts[1]), int(parts[2]))] = np.asarray([float(x) for x in parts[3:]], np.float64)
+        else:
+            k, v = [s.strip() for s in line.split("=", 1)]
+            kv[k] = v
+    return kv, vel
+
+
+def input_fingerprints(logical: dict, inp: dict) -> dict:
+    """float64 (sum, sum of squares) of the seeded step inputs, per tensor group: lets a test
+    tell a changed input stream from a changed result.  `logical` None: activations only."""
+    def acc(tensors):
+        s = q = 0.0
+        for t in tensors:
+            if t is None:
+                continue
+            d = t.double()
+            s += float(d.sum())
+            q += float((d * d).sum())
+        return s, q
+    groups = {
+        "img_tokens": [inp["img_tokens"]],
+        "ref_tokens": [inp["ref_tokens"]],
+        "txt_emb": [inp["txt_emb"]],
+    }
+    if logical is not None:
+        groups.update({
+            "mod": list(logical["mod"].values()),
+            "embedders": [logical["x_emb"], logical["ctx_emb"], logical["proj_out"]],
+            "dual": [t for pair in logical["dual"] for sw in pair for t in sw.values()],
+            "single": [t for sw in logical["single"] for t in sw.values()],
+        })
+    return {k: acc(v) for k, v in groups.items()}

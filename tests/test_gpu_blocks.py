@@ -6,6 +6,8 @@ Batch rows are independent ("FLUX.2 [klein] 4B/9B + Z-Image-Turbo on a shared Di
 scaffold": rows independent of their batch neighbours bit for bit), so at batch 4 the
 oracle checks rows 0 and 3 and the GPU's own batch invariance covers the rest.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -16,6 +18,7 @@ import helpers as Hx
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 BLOCK_ATOL, BLOCK_COS, STEP_COS = 3e-2, 0.999, 0.995
 # e4m3 keeps 3 mantissa bits (relative rounding up to 2^-4, rms 2^-4/sqrt(3) per operand):
 # each product of two quantised operands carries ~5 % rms relative error, so the
@@ -186,15 +189,35 @@ def test_step_klein_1024(dit):
     assert cs8 >= FP8_STEP_COS
 
 
-def test_step_batch_invariance_ref_b4(dit):
-    """Row b of the batch-4 reference-guided step equals the batch-1 step of row b, bit for bit."""
+def test_step_ref_b4_against_oracle_and_batch_invariance(dit):
+    """The whole reference-guided batch-4 step (1920x1088 target, one 1024x1024 reference,
+    N = 12768, a different sigma per row): rows 0 and 3 against the fp32 oracle's velocity
+    (sampled tokens and whole-row statistics, written by make_ref_step_golden.py), and row b
+    of the batch equal to the batch-1 step of row b, bit for bit."""
+    kv, want = Hx.read_step_golden(os.path.join(GOLDEN, "step_ref_1920x1088_rows0_3.txt"))
     wl = synth.WORKLOADS["ref_1920x1088_b4"]
-    logical = synth.model_weights(wl.widths, seed=5, device=DEV)
-    inp = synth.step_inputs(wl, seed=5, device=DEV)
-    inp["sigma"] = torch.tensor([0.9, 0.7, 0.55, 0.95], dtype=torch.float32, device=DEV)
+    seed = int(kv["seed"])
+    logical = synth.model_weights(wl.widths, seed=seed)
+    inp = synth.step_inputs(wl, seed=seed)
+    inp["sigma"] = torch.tensor([float(x) for x in kv["sigma"].split()], dtype=torch.float32)
+    # The CPU generators must give the inputs the oracle saw; a few last-place differences
+    # between platforms' samplers would move these sums by far less than the tolerance.
+    mine = Hx.input_fingerprints(logical, inp)
+    for k, (s, q) in mine.items():
+        ws, wq = (float(x) for x in kv[f"fingerprint.{k}"].split())
+        assert abs(s - ws) <= 0.05 and abs(q - wq) <= 1e-5 * wq, (k, s, ws, q, wq)
     vel, W = _step(dit, wl, logical, inp)
     assert torch.isfinite(vel.float()).all()
-    for b in (0, 3):
+    got = Hx.to_np(vel)
+    toks = [int(t) for t in kv["tokens"].split()]
+    for b in (int(r) for r in kv["rows"].split()):
+        g = got[b, toks]
+        w = np.stack([want[(b, t)] for t in toks])
+        cs, rms = Hx.cosine(g, w), float(np.sqrt((got[b] ** 2).mean()))
+        w_rms = float(kv[f"row{b}.rms"])
+        print(f"ref b4 row {b}: sampled cos {cs:.6f} max_abs {Hx.max_abs(g, w):.4g} rms {rms:.5f} (oracle {w_rms:.5f})")
+        assert cs >= STEP_COS, (b, cs)
+        assert abs(rms - w_rms) <= 1e-2 * w_rms, (b, rms, w_rms)
         wl1 = synth.Workload("row", wl.widths, 1, wl.n_txt, wl.grid, wl.ref_grids)
         one = {k: (v[b:b + 1].clone() if v is not None else None) for k, v in inp.items()}
         v1, _ = _step(dit, wl1, logical, one, W)
