@@ -78,66 +78,74 @@ def generator(seed: int, device="cpu") -> torch.Generator:
     return g
 
 
-def normal(shape, std, gen, device="cpu", mean=0.0) -> torch.Tensor:
-    """N(mean, std^2) rounded to bf16."""
-    t = torch.randn(*shape, generator=gen, device=device, dtype=torch.float32)
+def normal(shape, std, gen, device="cpu", mean=0.0, draw_dtype=torch.float32) -> torch.Tensor:
+    """N(mean, std^2) rounded to bf16.
+
+    draw_dtype float64 (about 4x slower on the CPU) gives the same bf16 values on every host:
+    torch's float32 CPU sampler rounds its transform differently on x86 and on Arm, which
+    moves some values by one bf16 step; a float64 draw would have to land within about
+    2^-44 of a bf16 rounding boundary for that to happen."""
+    t = torch.randn(*shape, generator=gen, device=device, dtype=draw_dtype)
     return (t * std + mean).to(torch.bfloat16)
 
 
-def mod_weights(wd: Widths, gen, device="cpu") -> dict:
+def mod_weights(wd: Widths, gen, device="cpu", draw_dtype=torch.float32) -> dict:
     H = wd.hidden
     return {
-        "t_in": normal((H, wd.time_dim), WEIGHT_STD, gen, device),
-        "t_out": normal((H, H), WEIGHT_STD, gen, device),
-        "mod": normal((17 * H, H), WEIGHT_STD, gen, device),
+        "t_in": normal((H, wd.time_dim), WEIGHT_STD, gen, device, draw_dtype=draw_dtype),
+        "t_out": normal((H, H), WEIGHT_STD, gen, device, draw_dtype=draw_dtype),
+        "mod": normal((17 * H, H), WEIGHT_STD, gen, device, draw_dtype=draw_dtype),
     }
 
 
-def stream_weights(wd: Widths, gen, device="cpu") -> dict:
+def stream_weights(wd: Widths, gen, device="cpu", draw_dtype=torch.float32) -> dict:
     H, F, D = wd.hidden, wd.mlp_hidden, wd.head_dim
     return {
-        "qkv": normal((3 * H, H), WEIGHT_STD, gen, device),
-        "q_norm": normal((D,), WEIGHT_STD, gen, device, mean=1.0),
-        "k_norm": normal((D,), WEIGHT_STD, gen, device, mean=1.0),
-        "out": normal((H, H), WEIGHT_STD, gen, device),
-        "mlp_in": normal((2 * F, H), WEIGHT_STD, gen, device),
-        "mlp_out": normal((H, F), WEIGHT_STD, gen, device),
+        "qkv": normal((3 * H, H), WEIGHT_STD, gen, device, draw_dtype=draw_dtype),
+        "q_norm": normal((D,), WEIGHT_STD, gen, device, mean=1.0, draw_dtype=draw_dtype),
+        "k_norm": normal((D,), WEIGHT_STD, gen, device, mean=1.0, draw_dtype=draw_dtype),
+        "out": normal((H, H), WEIGHT_STD, gen, device, draw_dtype=draw_dtype),
+        "mlp_in": normal((2 * F, H), WEIGHT_STD, gen, device, draw_dtype=draw_dtype),
+        "mlp_out": normal((H, F), WEIGHT_STD, gen, device, draw_dtype=draw_dtype),
     }
 
 
-def single_weights(wd: Widths, gen, device="cpu") -> dict:
+def single_weights(wd: Widths, gen, device="cpu", draw_dtype=torch.float32) -> dict:
     H, F, D = wd.hidden, wd.mlp_hidden, wd.head_dim
     return {
-        "qkv_mlp": normal((3 * H + 2 * F, H), WEIGHT_STD, gen, device),
-        "q_norm": normal((D,), WEIGHT_STD, gen, device, mean=1.0),
-        "k_norm": normal((D,), WEIGHT_STD, gen, device, mean=1.0),
-        "out": normal((H, H + F), WEIGHT_STD, gen, device),
+        "qkv_mlp": normal((3 * H + 2 * F, H), WEIGHT_STD, gen, device, draw_dtype=draw_dtype),
+        "q_norm": normal((D,), WEIGHT_STD, gen, device, mean=1.0, draw_dtype=draw_dtype),
+        "k_norm": normal((D,), WEIGHT_STD, gen, device, mean=1.0, draw_dtype=draw_dtype),
+        "out": normal((H, H + F), WEIGHT_STD, gen, device, draw_dtype=draw_dtype),
     }
 
 
-def model_weights(wd: Widths, seed: int, device="cpu", n_dual=None, n_single=None) -> dict:
+def model_weights(wd: Widths, seed: int, device="cpu", n_dual=None, n_single=None,
+                  draw_dtype=torch.float32) -> dict:
     """Every weight of the model, logical layouts, bf16."""
     g = generator(seed, device)
     H, C = wd.hidden, wd.in_channels
-    w = {"mod": mod_weights(wd, g, device),
-         "x_emb": normal((H, C), WEIGHT_STD, g, device),
-         "ctx_emb": normal((H, wd.txt_dim), WEIGHT_STD, g, device),
-         "proj_out": normal((C, H), WEIGHT_STD, g, device)}
+    w = {"mod": mod_weights(wd, g, device, draw_dtype=draw_dtype),
+         "x_emb": normal((H, C), WEIGHT_STD, g, device, draw_dtype=draw_dtype),
+         "ctx_emb": normal((H, wd.txt_dim), WEIGHT_STD, g, device, draw_dtype=draw_dtype),
+         "proj_out": normal((C, H), WEIGHT_STD, g, device, draw_dtype=draw_dtype)}
     nd = wd.n_dual if n_dual is None else n_dual
     ns = wd.n_single if n_single is None else n_single
-    w["dual"] = [(stream_weights(wd, g, device), stream_weights(wd, g, device)) for _ in range(nd)]
-    w["single"] = [single_weights(wd, g, device) for _ in range(ns)]
+    w["dual"] = [(stream_weights(wd, g, device, draw_dtype=draw_dtype),
+                  stream_weights(wd, g, device, draw_dtype=draw_dtype)) for _ in range(nd)]
+    w["single"] = [single_weights(wd, g, device, draw_dtype=draw_dtype) for _ in range(ns)]
     return w
 
 
-def step_inputs(wl: Workload, seed: int, device="cpu") -> dict:
+def step_inputs(wl: Workload, seed: int, device="cpu", draw_dtype=torch.float32) -> dict:
     """Activations of one step: latent tokens, reference tokens, text features, sigma."""
     g = generator(seed + 1000, device)
     wd = wl.widths
     out = {
-        "img_tokens": normal((wl.batch, wl.n_img, wd.in_channels), 1.0, g, device),
-        "ref_tokens": normal((wl.batch, wl.n_ref, wd.in_channels), 1.0, g, device) if wl.n_ref else None,
-        "txt_emb": normal((wl.batch, wl.n_txt, wd.txt_dim), 1.0, g, device),
+        "img_tokens": normal((wl.batch, wl.n_img, wd.in_channels), 1.0, g, device, draw_dtype=draw_dtype),
+        "ref_tokens": (normal((wl.batch, wl.n_ref, wd.in_channels), 1.0, g, device, draw_dtype=draw_dtype)
+                       if wl.n_ref else None),
+        "txt_emb": normal((wl.batch, wl.n_txt, wd.txt_dim), 1.0, g, device, draw_dtype=draw_dtype),
     }
     # reading R19: sigma_0 drawn from the seed in (0.5, 1]; one sigma per batch row
     s0 = 1.0 - 0.5 * torch.rand(1, generator=g, device=device, dtype=torch.float64).item()

@@ -10,11 +10,12 @@ What is stored (all from `oracle/`, nothing from the CUDA path):
   * the seed, the per-row sigma and the sampled target tokens;
   * per input tensor group, the float64 sum and sum of squares of the bf16 values that
     the seeded CPU generators produce, so that the test can tell a changed input stream
-    from a changed result;
+    from a changed result.  The inputs are drawn in float64 before the bf16 rounding, which
+    makes them the same on x86 and Arm hosts (the float32 sampler differs in the last place);
   * per checked row, the mean and rms of the whole velocity [8160, 128];
   * per checked row, the velocity of the sampled tokens (128 channels each).
 
-Run from the repository root (about ten minutes of CPU and 30 GB of host memory):
+Run from the repository root (about 30 minutes of CPU on 8 cores, 20 GB of host memory):
     python tests/golden/make_ref_step_golden.py
 """
 from __future__ import annotations
@@ -48,8 +49,8 @@ def sampled_tokens(n_img: int) -> np.ndarray:
 def main():
     wl = synth.WORKLOADS["ref_1920x1088_b4"]
     t0 = time.time()
-    logical = synth.model_weights(wl.widths, seed=SEED)
-    inp = synth.step_inputs(wl, seed=SEED)
+    logical = synth.model_weights(wl.widths, seed=SEED, draw_dtype=torch.float64)
+    inp = synth.step_inputs(wl, seed=SEED, draw_dtype=torch.float64)
     inp["sigma"] = torch.tensor(SIGMA, dtype=torch.float32)
     fp = Hx.input_fingerprints(logical, inp)
     print(f"inputs {time.time() - t0:.1f} s", flush=True)
@@ -63,6 +64,7 @@ def main():
         "# Expected velocity of the reference-guided batch-4 step (1920x1088 target, one 1024x1024",
         "# reference, 512 text rows, N = 12768, klein widths), batch rows 0 and 3, from the fp32 oracle.",
         "# Written by tests/golden/make_ref_step_golden.py (calls the seeded generators and oracle/ only).",
+        "# Inputs: synth.model_weights / step_inputs with draw_dtype float64.",
         f"seed = {SEED}",
         "sigma = " + " ".join(repr(float(s)) for s in SIGMA),
         "rows = " + " ".join(str(r) for r in ROWS),

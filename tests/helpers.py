@@ -108,3 +108,15 @@ def input_fingerprints(logical: dict, inp: dict) -> dict:
             "single": [t for sw in logical["single"] for t in sw.values()],
         })
     return {k: acc(v) for k, v in groups.items()}
+
+
+def check_fingerprints(mine: dict, kv: dict):
+    """Compare input fingerprints with a golden's `fingerprint.<group> = sum sumsq` lines.
+
+    The bounds allow for float64 summation order only (about 1e-12 relative).  A different
+    stream moves the sum by about sqrt(sumsq) and the sum of squares by about
+    sqrt(2/n) relative; the last-place drift of a float32 sampler across hosts moved the sum
+    of 4.2 M latent values by ~4e-5 sqrt(sumsq)."""
+    for k, (s, q) in mine.items():
+        ws, wq = (float(x) for x in kv[f"fingerprint.{k}"].split())
+        assert abs(s - ws) <= 1e-6 * wq ** 0.5 and abs(q - wq) <= 1e-10 * wq, (k, s, ws, q, wq)
