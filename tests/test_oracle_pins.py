@@ -278,7 +278,7 @@ def test_dual_block_attention_is_joint_and_streams_use_own_weights():
     cfg, wl, wi, wt, ws, x, m, c, s = _tiny_block_setup()
     mod = O.split_modulation(m, cfg.hidden)
     y = O.dual_block(x, wl.n_txt, wi, wt, mod, c, s, cfg)
-    x2 = x.copy(); x2[:, -1] += RNG.standard_normal(x.shape[-1])  # not a constant: LN ignores that                                    # perturb one reference row
+    x2 = x.copy(); x2[:, -1] += RNG.standard_normal(x.shape[-1])  # perturb one reference row (not by a constant: LN removes that)
     y2 = O.dual_block(x2, wl.n_txt, wi, wt, mod, c, s, cfg)
     assert np.abs(y2[:, 0] - y[:, 0]).max() > 1e-6                     # text row sees it
     # swapping the text weights changes only... everything (joint attention), but the
@@ -302,6 +302,114 @@ def test_single_block_zero_gate_and_permutation_equivariance():
     y = O.single_block(x, ws, mod, c1, s1, cfg)
     yp = O.single_block(x[:, perm], ws, mod, c1, s1, cfg)
     np.testing.assert_allclose(yp, y[:, perm], rtol=1e-10, atol=1e-10)
+
+
+def _layer_norm_textbook(x, eps=1e-6):
+    mu = x.mean(-1, keepdims=True)
+    return (x - mu) / np.sqrt(((x - mu) ** 2).mean(-1, keepdims=True) + eps)
+
+
+def _permutation(n, rng):
+    """A permutation p with p != p^-1, and the [out, in] matrix P of the map o -> o[p]."""
+    while True:
+        p = rng.permutation(n)
+        if (p != np.argsort(p)).any():
+            break
+    P = np.zeros((n, n))
+    P[np.arange(n), p] = 1.0
+    return p, P
+
+
+def test_dual_block_uniform_attention_closed_form():
+    """Zero q and k rows make every score 0, so attention is the mean of V over all N joint
+    rows (both streams); with out = a permutation matrix, zero MLP-out and zero shift/scale,
+    each row must be x + gate_a * o[p].  Pins the V slice of the qkv weight, joint attention,
+    each stream's gate slot and own weights, and the [out, in] orientation of a square
+    projection (y W^T: a transposed W gives o[p^-1])."""
+    cfg, wl, wi, wt, ws, x, m, c, s = _tiny_block_setup()
+    H, n_txt = cfg.hidden, wl.n_txt
+    rng = np.random.default_rng(11)
+    (p_i, P_i), (p_t, P_t) = _permutation(H, rng), _permutation(H, rng)
+
+    def prep(w, P):
+        qkv = w.qkv.copy()
+        qkv[:2 * H] = 0
+        return O.StreamWeights(**{**w.__dict__, "qkv": qkv, "out": P, "mlp_out": np.zeros_like(w.mlp_out)})
+
+    m2 = m.copy()
+    m2[:, 0:2 * H] = 0          # image stream shift_a, scale_a
+    m2[:, 6 * H:8 * H] = 0      # text stream shift_a, scale_a
+    y = O.dual_block(x, n_txt, prep(wi, P_i), prep(wt, P_t), O.split_modulation(m2, H), c, s, cfg)
+    ln = _layer_norm_textbook(x)
+    v = np.concatenate([ln[:, :n_txt] @ wt.qkv[2 * H:].T, ln[:, n_txt:] @ wi.qkv[2 * H:].T], axis=1)
+    o = v.mean(axis=1, keepdims=True)
+    want_t = x[:, :n_txt] + m[:, None, 8 * H:9 * H] * o[..., p_t]
+    want_i = x[:, n_txt:] + m[:, None, 2 * H:3 * H] * o[..., p_i]
+    np.testing.assert_allclose(y[:, :n_txt], want_t, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(y[:, n_txt:], want_i, rtol=0, atol=1e-12)
+
+
+def test_single_block_uniform_attention_closed_form():
+    """The single-stream block under the same construction: q, k and MLP-gate rows of the
+    fused projection zero (silu(0) = 0, so act = 0 whatever the up rows), the attention part
+    of out a permutation: x + gate * o[p].  Pins the column order [q | k | v | gate | up] of
+    the fused projection and the [attn | act] order and orientation of the out-projection."""
+    cfg, wl, wi, wt, ws, x, m, c, s = _tiny_block_setup(ref=())
+    H, F = cfg.hidden, cfg.mlp_hidden
+    p, P = _permutation(H, np.random.default_rng(12))
+    qkv_mlp = ws.qkv_mlp.copy()
+    qkv_mlp[:2 * H] = 0
+    qkv_mlp[3 * H:3 * H + F] = 0
+    out = ws.out.copy()
+    out[:, :H] = P
+    ws2 = O.SingleWeights(**{**ws.__dict__, "qkv_mlp": qkv_mlp, "out": out})
+    m2 = m.copy()
+    m2[:, 12 * H:14 * H] = 0
+    y = O.single_block(x, ws2, O.split_modulation(m2, H), c, s, cfg)
+    o = (_layer_norm_textbook(x) @ ws.qkv_mlp[2 * H:3 * H].T).mean(axis=1, keepdims=True)
+    np.testing.assert_allclose(y, x + m[:, None, 14 * H:15 * H] * o[..., p], rtol=0, atol=1e-12)
+
+
+def test_blocks_mlp_gate_is_the_first_half():
+    """Reading R9 (first half of the MLP-in rows is the gate): with coordinate 0 of every row
+    12 above the rest, LN puts it near +9, so gate rows -10 e_0 give silu(< -60) < 1e-24 and
+    the MLP adds nothing, whatever the up rows; the same rows in the up half leave the MLP on.
+    V rows are zeroed so the attention adds nothing either."""
+    cfg, wl, wi, wt, ws, x, m, c, s = _tiny_block_setup()
+    H, F, n_txt = cfg.hidden, cfg.mlp_hidden, wl.n_txt
+    x2 = x.copy()
+    x2[..., 0] += 12.0
+    assert _layer_norm_textbook(x2)[..., 0].min() > 6.0
+
+    def dual_w(w, off_half):
+        qkv = w.qkv.copy()
+        qkv[2 * H:] = 0
+        mi = w.mlp_in.copy()
+        rows = slice(0, F) if off_half == "gate" else slice(F, 2 * F)
+        mi[rows] = 0
+        mi[rows, 0] = -10.0
+        return O.StreamWeights(**{**w.__dict__, "qkv": qkv, "mlp_in": mi})
+
+    mod = O.split_modulation(m, H)
+    y = O.dual_block(x2, n_txt, dual_w(wi, "gate"), dual_w(wt, "gate"), mod, c, s, cfg)
+    np.testing.assert_allclose(y, x2, rtol=0, atol=1e-20)
+    y_up = O.dual_block(x2, n_txt, dual_w(wi, "up"), dual_w(wt, "up"), mod, c, s, cfg)
+    assert np.abs(y_up - x2).max() > 1e-2
+
+    cfg1, wl1, _, _, ws1, x1, m1, c1, s1 = _tiny_block_setup(ref=())
+    x1[..., 0] += 12.0
+
+    def single_w(off_half):
+        w = ws1.qkv_mlp.copy()
+        w[2 * H:3 * H] = 0
+        rows = slice(3 * H, 3 * H + F) if off_half == "gate" else slice(3 * H + F, 3 * H + 2 * F)
+        w[rows] = 0
+        w[rows, 0] = -10.0
+        return O.SingleWeights(**{**ws1.__dict__, "qkv_mlp": w})
+
+    mod1 = O.split_modulation(m1, H)
+    np.testing.assert_allclose(O.single_block(x1, single_w("gate"), mod1, c1, s1, cfg1), x1, rtol=0, atol=1e-20)
+    assert np.abs(O.single_block(x1, single_w("up"), mod1, c1, s1, cfg1) - x1).max() > 1e-2
 
 
 def test_blocks_batch_rows_independent():
