@@ -237,6 +237,23 @@ def test_modulation_slots_and_zero_input_path():
     np.testing.assert_array_equal(m2[0], m2[1])
 
 
+def test_modulation_closed_form_at_sigma_zero():
+    """At sigma = 0 the sinusoid is [1 ... 1 | 0 ... 0].  With W_in putting c_r on the first
+    cosine column of row r, W_out = I and W_mod = 17 stacked identities, every slot of m must
+    be silu(silu(c)) (the library SiLU): pins both SiLUs of the timestep MLP and the one
+    before the modulation projection."""
+    cfg = O.Config.tiny()
+    H = cfg.hidden
+    c = np.linspace(-4.0, 4.0, H)
+    w_in = np.zeros((H, 256))
+    w_in[:, 0] = c
+    w_mod = np.vstack([np.eye(H)] * 17)
+    m = O.modulation(np.array([0.0]), w_in, np.eye(H), w_mod, cfg)
+    silu = lambda t: torch.nn.functional.silu(torch.from_numpy(t)).numpy()
+    want = np.tile(silu(silu(c)), 17)
+    np.testing.assert_allclose(m[0], want, rtol=1e-12, atol=1e-15)
+
+
 # ------------------------------------------------------------------ blocks
 def _tiny_block_setup(seed=0, batch=1, n_txt=8, grid=(3, 4), ref=((2, 2),)):
     wd = synth.TINY
@@ -412,6 +429,36 @@ def test_blocks_mlp_gate_is_the_first_half():
     assert np.abs(O.single_block(x1, single_w("up"), mod1, c1, s1, cfg1) - x1).max() > 1e-2
 
 
+def test_dual_block_mlp_uses_its_own_modulation_slots():
+    """With the V rows zeroed the attention adds nothing, so the attention's shift and scale
+    (slots 0, 1, 6, 7) must not change the output at all, a zero MLP gate (slots 5, 11) must
+    leave x unchanged, and the MLP's shift (slots 3, 9) must matter."""
+    cfg, wl, wi, wt, ws, x, m, c, s = _tiny_block_setup()
+    H, n_txt = cfg.hidden, wl.n_txt
+
+    def no_v(w):
+        qkv = w.qkv.copy()
+        qkv[2 * H:] = 0
+        return O.StreamWeights(**{**w.__dict__, "qkv": qkv})
+
+    wi0, wt0 = no_v(wi), no_v(wt)
+    run = lambda mm: O.dual_block(x, n_txt, wi0, wt0, O.split_modulation(mm, H), c, s, cfg)
+    y = run(m)
+    m_a = m.copy()
+    for slot in (0, 1, 6, 7):
+        m_a[:, slot * H:(slot + 1) * H] += RNG.standard_normal((m.shape[0], H))
+    np.testing.assert_array_equal(run(m_a), y)
+    m_g = m.copy()
+    m_g[:, 5 * H:6 * H] = 0
+    m_g[:, 11 * H:12 * H] = 0
+    np.testing.assert_array_equal(run(m_g), x)
+    m_s = m.copy()
+    m_s[:, 3 * H:4 * H] += 1.0
+    m_s[:, 9 * H:10 * H] += 1.0
+    assert np.abs(run(m_s)[:, :n_txt] - y[:, :n_txt]).max() > 1e-4
+    assert np.abs(run(m_s)[:, n_txt:] - y[:, n_txt:]).max() > 1e-4
+
+
 def test_blocks_batch_rows_independent():
     cfg, wl, wi, wt, ws, x, m, c, s = _tiny_block_setup(batch=3)
     mod = O.split_modulation(m, cfg.hidden)
@@ -451,6 +498,25 @@ def test_step_uses_only_target_rows_and_ref_tokens_matter():
     a2 = list(a); a2[1] = a[1] + 1.0
     v2 = O.dit_step(ow, *a2)
     assert v.shape == v2.shape and np.abs(v - v2).max() > 1e-6
+
+
+def test_step_without_blocks_maps_each_target_token_to_its_own_velocity_row():
+    """With no blocks, nothing mixes rows: the text features must not touch the velocity,
+    and changing image token j must change velocity row j only (the final layer reads the
+    target rows, which follow the text rows)."""
+    wd, wl, w, inp, ids = _tiny_step()
+    ow = Hx.oracle_weights(wd, w)
+    img, ref, txt = Hx.to_np(inp["img_tokens"]), Hx.to_np(inp["ref_tokens"]), Hx.to_np(inp["txt_emb"])
+    sig = Hx.to_np(inp["sigma"])
+    step = lambda i, t: O.dit_step(ow, i, ref, t, sig, ids, n_dual=0, n_single=0)
+    v = step(img, txt)
+    np.testing.assert_array_equal(step(img, txt + 1.0), v)
+    j = 5
+    img2 = img.copy()
+    img2[:, j] += RNG.standard_normal(img.shape[-1])
+    d = np.abs(step(img2, txt) - v).max(axis=-1)
+    assert (d[:, j] > 1e-6).all()
+    assert (np.delete(d, j, axis=1) == 0).all()
 
 
 def test_euler_loop_telescopes_and_schedule_ends_at_zero():
