@@ -459,6 +459,30 @@ def test_dual_block_mlp_uses_its_own_modulation_slots():
     assert np.abs(run(m_s)[:, n_txt:] - y[:, n_txt:]).max() > 1e-4
 
 
+def test_dual_and_single_blocks_agree_on_the_attention_path():
+    """The two block forms compute the same attention sub-layer by separate code: a dual
+    block whose streams share one weight set and one modulation, with its MLP off (zero
+    MLP-out), must equal a single block with the same q/k/v/out weights and norm weights,
+    its MLP off (zero gate rows: act = silu(0) up = 0).  A slip in either path's q/k
+    handling (norm order, a swapped norm weight, RoPE missing or on one operand) breaks
+    the agreement; the shared helpers have their own pins."""
+    cfg, wl, wi, wt, ws, x, m, c, s = _tiny_block_setup()
+    H, F = cfg.hidden, cfg.mlp_hidden
+    sw = O.StreamWeights(qkv=ws.qkv_mlp[:3 * H].copy(), q_norm=ws.q_norm, k_norm=ws.k_norm,
+                         out=ws.out[:, :H].copy(), mlp_in=wi.mlp_in, mlp_out=np.zeros_like(wi.mlp_out))
+    m2 = m.copy()
+    for stream0 in (0, 6):                    # both streams' attention slots = the single slots
+        m2[:, stream0 * H:(stream0 + 3) * H] = m[:, 12 * H:15 * H]
+    qkv_mlp = ws.qkv_mlp.copy()
+    qkv_mlp[3 * H:3 * H + F] = 0
+    ws0 = O.SingleWeights(**{**ws.__dict__, "qkv_mlp": qkv_mlp})
+    mod = O.split_modulation(m2, H)
+    y_dual = O.dual_block(x, wl.n_txt, sw, sw, mod, c, s, cfg)
+    y_single = O.single_block(x, ws0, mod, c, s, cfg)
+    np.testing.assert_allclose(y_dual, y_single, rtol=0, atol=1e-12)
+    assert np.abs(y_single - x).max() > 1e-3   # the attention sub-layer is not trivial here
+
+
 def test_blocks_batch_rows_independent():
     cfg, wl, wi, wt, ws, x, m, c, s = _tiny_block_setup(batch=3)
     mod = O.split_modulation(m, cfg.hidden)
@@ -517,6 +541,9 @@ def test_step_without_blocks_maps_each_target_token_to_its_own_velocity_row():
     d = np.abs(step(img2, txt) - v).max(axis=-1)
     assert (d[:, j] > 1e-6).all()
     assert (np.delete(d, j, axis=1) == 0).all()
+    # the final layer normalises: scaling every target token by 3 scales each embedded row
+    # by 3, which LayerNorm removes (up to its eps against a row variance of ~0.05)
+    np.testing.assert_allclose(step(3.0 * img, txt), v, rtol=1e-3, atol=1e-4)
 
 
 def test_euler_loop_telescopes_and_schedule_ends_at_zero():
