@@ -584,6 +584,10 @@ def test_e4m3_known_encodings_ties_and_saturation():
     assert O.e4m3_encode(0.3) == 0x2A
     # saturation to the largest finite value instead of NaN / overflow
     assert O.e4m3_encode(464.0) == 0x7E and O.e4m3_encode(1e9) == 0x7E and O.e4m3_encode(-1e9) == 0xFE
+    assert O.e4m3_encode(470.0) == 0x7E and O.e4m3_encode(-447.0) == 0xFE
+    # zero keeps its sign, as in the IEEE formats: -0 and negative values that round to
+    # zero give the negative-zero code
+    assert O.e4m3_encode(-0.0) == 0x80 and O.e4m3_encode(-1e-6) == 0x80 and O.e4m3_encode(1e-6) == 0x00
 
 
 def test_e4m3_codes_round_trip_and_are_monotonic():
