@@ -75,6 +75,22 @@ def test_workspace_size_grows_with_shape(dit):
     assert a > N * H * 2 * 5 + N * (H + F) * 2
 
 
+def test_workspace_size_at_the_largest_accepted_shape_does_not_wrap(dit):
+    """Batch 64 and 2^20 tokens (the limits check_shape accepts) need ~10^14 bytes: the size
+    must come out as that (64-bit arithmetic), and one row or token more is rejected."""
+    c = dit.dit_config_klein()
+    n_txt, n_img = 512, (1 << 20) - 512
+    big = dit.dit_workspace_size(c, dit.make_shape(64, n_txt, n_img, 0))
+    B, N, H, F = 64, 1 << 20, 3072, 9216
+    assert big > B * N * (H + F) * 2 + B * N * H * 2 * 5
+    assert big < 1 << 50
+    assert big > dit.dit_workspace_size(c, dit.make_shape(63, n_txt, n_img, 0))
+    for shape, want in ((dit.make_shape(65, n_txt, n_img, 0), dit.DIT_ERR_INVALID_ARG),
+                        (dit.make_shape(1, n_txt, n_img + 1, 0), dit.DIT_ERR_UNSUPPORTED)):
+        n = C.c_size_t(0)
+        assert dit.lib().dit_workspace_size(C.byref(c), C.byref(shape), C.byref(n)) == want
+
+
 def test_unsupported_configs_rejected(dit):
     shape = dit.make_shape(1, 8, 16, 0)
     for field, val in (("head_dim", 64), ("hidden", 3000), ("mlp_hidden", 100), ("in_channels", 20),
