@@ -44,8 +44,9 @@ if ROOT not in sys.path:
 METRIC = "DiT steps/s at 1024² (512 txt + 4096 img tokens); TFLOP/s vs GB300 bf16 peak"
 UNIT = "steps/s"
 
-# Roofline denominators: the measured peaks of this GPU pool when the driver has written
-# them, else the recipe's fallback figures (reported as such).
+# Roofline denominators: the measured copy bandwidth and bf16 GEMM throughput in
+# MEASURED_PEAKS.json when that file is present, else these fallback figures (one earlier
+# GB300 measurement), reported as such.
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 # DRAM traffic per launch of the dominant kernel from one ncu capture (see profiles/);
