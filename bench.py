@@ -163,6 +163,19 @@ def gpu_id_for_smi(torch, dev_index):
 
 
 # ---------------------------------------------------------------------------------- ranks
+PG_TIMEOUT_S = 300.0
+
+
+def init_replica_group(backend: str, timeout_s: float = PG_TIMEOUT_S) -> None:
+    """Process group of the replicas (RANK, WORLD_SIZE and MASTER_* from the environment).
+    A replica that dies between steps makes the others' next collective (the barriers
+    around the timed region, the max over ranks) end with an error within timeout_s
+    instead of waiting without end."""
+    import datetime
+    import torch.distributed as tdist
+    tdist.init_process_group(backend, timeout=datetime.timedelta(seconds=timeout_s))
+
+
 def reduce_max(x: float, world: int, device) -> float:
     """Max of a per-rank scalar over all ranks (identity at world size 1)."""
     import torch
@@ -491,7 +504,7 @@ def main():
         import torch
         import torch.distributed as tdist
         torch.cuda.set_device(local_rank)
-        tdist.init_process_group("nccl")
+        init_replica_group("nccl")
     try:
         run_ours(args, wl, rank, world, local_rank)
     finally:
