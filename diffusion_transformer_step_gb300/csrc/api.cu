@@ -61,13 +61,16 @@ bool pdl_enabled() {
 }
 
 int sm_count() {
-  static int cached[16] = {0};
+  static std::atomic<int> cached[16];  // per device, filled by whichever host thread asks first
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 16 && cached[dev]) return cached[dev];
+  if (dev >= 0 && dev < 16) {
+    const int c = cached[dev].load(std::memory_order_relaxed);
+    if (c) return c;
+  }
   int n = 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
-  if (dev >= 0 && dev < 16) cached[dev] = n;
+  if (dev >= 0 && dev < 16) cached[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 

@@ -42,6 +42,8 @@
 // [256t + 128, 256t + 256).
 #include <math.h>
 
+#include <atomic>
+
 #include "runtime.h"
 
 namespace dit {
@@ -500,7 +502,8 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
   }
 }
 
-bool g_attr_set[16] = {false};
+// the shared-memory attribute has been raised on device d (set from any host thread)
+std::atomic<bool> g_attr_set[16];
 
 }  // namespace
 
@@ -526,11 +529,11 @@ cudaError_t launch_attention(int batch, int heads, int n, const bf16* q, const b
   P.status = status;
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 16 && !g_attr_set[dev]) {
+  if (dev < 16 && !g_attr_set[dev].load(std::memory_order_acquire)) {
     cudaError_t e =
         cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    g_attr_set[dev] = true;
+    g_attr_set[dev].store(true, std::memory_order_release);
   }
   dim3 grid((n + 2 * kBQ - 1) / (2 * kBQ), heads, batch);
   LaunchScope scope(kClsAttention, s);

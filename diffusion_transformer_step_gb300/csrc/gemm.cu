@@ -35,6 +35,8 @@
 //   QKV       columns [0, 3H): per-head RMSNorm (fp32, eps) * w, RoPE on adjacent pairs
 //             from the fp32 table, written head-major [B, heads, seq, 128]; columns
 //             >= 3H: SWIGLU into the concat buffer (single-stream fused projection).
+#include <atomic>
+
 #include "runtime.h"
 
 namespace dit {
@@ -571,7 +573,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 }
 
-bool g_attr_set[32] = {false};
+// the shared-memory attribute has been raised for (device, operand type) (any host thread)
+std::atomic<bool> g_attr_set[32];
 
 }  // namespace
 
@@ -668,13 +671,13 @@ cudaError_t launch_gemm(const GemmProblemHost* probs, int nprob, int batch, floa
   cudaGetDevice(&dev);
   const bool fp8 = probs[0].fp8 != 0;
   const int slot = dev * 2 + (fp8 ? 1 : 0);
-  if (dev < 16 && !g_attr_set[slot]) {
+  if (dev < 16 && !g_attr_set[slot].load(std::memory_order_acquire)) {
     cudaError_t e = fp8 ? cudaFuncSetAttribute(gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                (int)kSmemBytes)
                         : cudaFuncSetAttribute(gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    g_attr_set[slot] = true;
+    g_attr_set[slot].store(true, std::memory_order_release);
   }
   const int pairs_max = sm_count() / 2;
   const int pairs = tiles < pairs_max ? tiles : pairs_max;

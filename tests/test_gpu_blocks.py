@@ -350,3 +350,44 @@ def test_dual_block_fp8(dit, wl):
     MLP-in on adaLN's quantised output, out and MLP-out on the quantised attention output and
     activations) against the oracle."""
     run_block(dit, "dual", wl, seed=0, fp8="all")
+
+
+def test_concurrent_steps_from_two_host_threads(dit):
+    """Calls on different workspaces and streams may run concurrently from different host
+    threads: two threads, each with its own stream, workspace and inputs, run 20 steps each
+    at once on shared weights; every result equals the one-thread result bit for bit."""
+    import threading
+    wl = TINY_REF
+    logical = synth.model_weights(wl.widths, seed=12)
+    W = dit.DeviceWeights(wl.widths, logical)
+    inps = [synth.step_inputs(wl, seed=20 + i) for i in range(2)]
+    want = [_step(dit, wl, logical, inp, W)[0] for inp in inps]
+    shape, rope, _, nbytes = _setup(dit, wl, W)
+    bufs = []
+    for inp in inps:
+        d = {k: (v.to(DEV) if v is not None else None) for k, v in inp.items()}
+        vel = torch.empty((wl.batch, wl.n_img, wl.widths.in_channels), dtype=torch.bfloat16, device=DEV)
+        bufs.append((torch.zeros(nbytes, dtype=torch.uint8, device=DEV), vel, d, torch.cuda.Stream()))
+    torch.cuda.synchronize()
+    errors = []
+
+    def work(i):
+        ws, vel, d, s = bufs[i]
+        try:
+            for _ in range(20):
+                dit.dit_step_fwd(W.w, shape, d["img_tokens"], d["ref_tokens"], d["txt_emb"], rope, d["sigma"], vel,
+                                 ws, nbytes, s)
+            s.synchronize()
+        except Exception as e:  # reported below, in the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(120)
+    assert not errors, errors
+    for i, (ws, vel, _, s) in enumerate(bufs):
+        st, where = dit.dit_sync_status(ws, s)
+        assert st == dit.DIT_OK, f"device wait gave up at site {where:#x}"
+        assert torch.equal(vel, want[i]), i
