@@ -186,3 +186,56 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch, dit):
     monkeypatch.setattr(mod, "_lib", None)
     with pytest.raises(RuntimeError):
         mod.lib()
+
+
+def test_loop_host_graph_and_helper_calls_validate_before_any_cuda_call(dit):
+    """On a host without a GPU any CUDA call fails, so each of these returning its own
+    validation status (not DIT_ERR_CUDA), with the launch counter unmoved, shows that the
+    denoising loop, the host-buffer step, graph capture, weight quantisation, the self-test
+    and the status read check their arguments before touching the device."""
+    L = dit.lib()
+    before = dit.dit_launch_count()
+    fake = 0x10000
+    c = dit.dit_config_klein()
+    c.n_dual, c.n_single = 0, 0
+    w = dit.dit_weights()
+    w.cfg = c
+    w.mod.t_in = w.mod.t_out = w.mod.mod = fake
+    w.x_emb = w.ctx_emb = w.proj_out = fake
+    shape = dit.make_shape(1, 512, 4096, 0)
+    ref_shape = dit.make_shape(1, 512, 4096, 1024)
+    big = 1 << 40
+    sig = (C.c_float * 9)(*([0.9, 0.7, 0.5, 0.2, 0.0] + [0.0] * 4))
+    bad_sig = (C.c_float * 9)(*([0.9, 1500.0, 0.5, 0.2, 0.0] + [0.0] * 4))
+    INV, WS = dit.DIT_ERR_INVALID_ARG, dit.DIT_ERR_WORKSPACE
+    den = lambda sh, ref, sg, steps, nbytes: L.dit_denoise_fwd(C.byref(w), C.byref(sh), fake, ref, fake, fake, sg,
+                                                               steps, fake, nbytes, None)
+    assert den(shape, None, sig, 0, big) == INV            # at least one step
+    assert den(shape, None, sig, 9, big) == INV            # at most eight
+    assert den(shape, None, bad_sig, 4, big) == INV        # sigma outside [0, 1000]
+    assert den(shape, None, None, 4, big) == INV           # no schedule
+    assert den(ref_shape, None, sig, 4, big) == INV        # reference rows without reference tokens
+    assert den(shape, fake, sig, 4, big) == INV            # reference tokens without reference rows
+    assert den(shape, None, sig, 4, 4096) == WS
+    host = lambda sh, ref, nbytes: L.dit_step_host(C.byref(w), C.byref(sh), fake, ref, fake, fake, fake, fake, fake,
+                                                   nbytes, None)
+    assert host(ref_shape, None, big) == INV
+    assert host(shape, None, 4096) == WS
+    assert L.dit_step_host(C.byref(w), C.byref(shape), None, None, fake, fake, fake, fake, fake, big, None) == INV
+    g = C.c_void_p(123)
+    assert L.dit_step_graph_create(C.byref(w), C.byref(shape), fake, None, fake, fake, fake, fake, fake, 4096, 0, None,
+                                   C.byref(g)) == WS
+    assert g.value is None                                  # no graph handle on failure
+    assert L.dit_step_graph_create(C.byref(w), C.byref(shape), fake, None, fake, fake, fake, fake, fake, big, 0, None,
+                                   None) == INV
+    assert L.dit_graph_launch(None, None) == INV
+    assert L.dit_graph_destroy(None) == dit.DIT_OK
+    assert L.dit_quantize_rows_fp8(fake, 4, 24, fake, fake, None) == INV       # cols % 16
+    assert L.dit_quantize_rows_fp8(fake, 4, 32, fake, fake + 4, None) == INV   # misaligned scales
+    assert L.dit_quantize_rows_fp8(fake, 0, 32, fake, fake, None) == INV
+    assert L.dit_selftest_wait_timeout(fake, 256, 0, None) == INV
+    assert L.dit_selftest_wait_timeout(fake, 256, 2000000, None) == INV
+    assert L.dit_selftest_wait_timeout(fake, 8, 100, None) == INV
+    assert L.dit_sync_status(None, None, None) == INV
+    assert L.dit_sync_status(fake + 8, None, None) == INV
+    assert dit.dit_launch_count() == before
