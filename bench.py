@@ -93,6 +93,41 @@ def class_flops(wd, batch, n_txt, n_img, n_ref):
     }
 
 
+def step_class_bytes(wd, batch, n_txt, n_img, n_ref):
+    """Algorithmic DRAM bytes per step of the HBM-bound kernel classes.
+    adaln: every pass reads its input rows once and writes the bf16 output once (the dual
+    block's second pass reads the fp32 midpoint residual; the final pass covers the target
+    rows only); the per-row modulation vectors are a few KB and not counted.
+    modulation_gemv: the timestep-MLP and modulation weights read once (bf16)."""
+    H = wd.hidden
+    N = n_txt + n_img + n_ref
+    row16 = N * H * 2
+    adaln = batch * (wd.n_dual * (2 * row16 + (N * H * 4 + row16)) + wd.n_single * 2 * row16
+                     + 2 * n_img * H * 2)
+    modulation = (H * wd.time_dim + H * H + 17 * H * H) * 2
+    return {"adaln": float(adaln), "modulation_gemv": float(modulation)}
+
+
+def kernel_breakdown(ms_by_class, flops_per_launch, bytes_per_step, n_steps, hbm_peak_gbs):
+    """Per kernel class, from its launch times (ms) over n_steps steps: launches, total and
+    mean time, share of the device time; TFLOP/s for the contractions (FLOPs per launch /
+    mean time) and GB/s with the fraction of the HBM peak for the HBM-bound classes (bytes
+    per step x n_steps / total time)."""
+    total = sum(sum(v) for v in ms_by_class.values())
+    out = {}
+    for k, v in ms_by_class.items():
+        ms = sum(v)
+        e = {"launches": len(v), "ms_total": round(ms, 4), "ms_mean": round(ms / len(v), 5),
+             "share": round(ms / total, 4) if total else None}
+        if k in flops_per_launch:
+            e["tflops"] = round(flops_per_launch[k] / (ms / len(v) / 1e3) / 1e12, 1)
+        if k in bytes_per_step and ms > 0:
+            e["gbs"] = round(bytes_per_step[k] * n_steps / (ms / 1e3) / 1e9, 1)
+            e["frac_of_hbm"] = round(e["gbs"] / hbm_peak_gbs, 4) if hbm_peak_gbs else None
+        out[k] = e
+    return out
+
+
 def step_flops(wd, batch, n_txt, n_img, n_ref):
     H, F, C = wd.hidden, wd.mlp_hidden, wd.in_channels
     N = n_txt + n_img + n_ref
@@ -425,12 +460,8 @@ def run_ours(args, wl, rank, world, local_rank):
 
     # ---- roofline of the dominant kernel class (its launches timed inside the timed region)
     peaks, src = load_peaks()
-    total_bd = sum(sum(v) for v in bd_by_cls.values())
-    kernels = {k: {"launches": len(v), "ms_total": round(sum(v), 4), "ms_mean": round(sum(v) / len(v), 5),
-                   "share": round(sum(v) / total_bd, 4) if total_bd else None} for k, v in bd_by_cls.items()}
-    for k, v in kernels.items():
-        if k in flops_cls:
-            v["tflops"] = round(flops_cls[k] / (v["ms_mean"] / 1e3) / 1e12, 1)
+    kernels = kernel_breakdown(bd_by_cls, flops_cls, step_class_bytes(wd, wl.batch, wl.n_txt, wl.n_img, wl.n_ref),
+                               bd_steps, peak_get(peaks, "hbm_gbs"))
     dom_ms = [t for name, t in records if name == dom]
     mean_ms = sum(dom_ms) / len(dom_ms)
     achieved = flops_cls[dom] / (mean_ms / 1e3) / 1e12

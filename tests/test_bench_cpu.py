@@ -37,3 +37,28 @@ def test_timing_select_rejects_an_empty_mask():
     L = dit.lib()
     assert L.dit_timing_select(0) == dit.DIT_ERR_INVALID_ARG
     assert L.dit_timing_select(0xFFFFFFFF) == dit.DIT_OK
+
+
+def test_hbm_class_bytes_of_the_1024_step():
+    """adaLN: 5 dual blocks x (bf16 pass 4NH + fp32-input pass 6NH) + 20 single x 4NH + the
+    final pass over the 4096 target rows (4 x 4096 x H); modulation: the 256->H, H->H and
+    H->17H weights in bf16.  N = 4608, H = 3072."""
+    wl = synth.WORKLOADS["step_1024"]
+    b = bench.step_class_bytes(wl.widths, wl.batch, wl.n_txt, wl.n_img, wl.n_ref)
+    assert b["adaln"] == 707_788_800 + 1_132_462_080 + 50_331_648
+    assert b["modulation_gemv"] == 341_311_488
+    b4 = bench.step_class_bytes(wl.widths, 4, wl.n_txt, wl.n_img, wl.n_ref)
+    assert b4["adaln"] == 4 * b["adaln"] and b4["modulation_gemv"] == b["modulation_gemv"]
+
+
+def test_kernel_breakdown_rates_and_shares():
+    recs = {"adaln": [0.02] * 62, "gemm_fused_qkv_mlp": [0.43] * 40, "attention": [0.2] * 50}
+    flops = {"gemm_fused_qkv_mlp": 7.83e11, "attention": 2.609e11}
+    k = bench.kernel_breakdown(recs, flops, {"adaln": 1.8906e9}, 2, 6800.0)
+    assert k["adaln"]["launches"] == 62 and k["adaln"]["ms_total"] == pytest.approx(1.24)
+    assert k["adaln"]["gbs"] == pytest.approx(1.8906e9 * 2 / 1.24e-3 / 1e9, abs=0.1)
+    assert k["adaln"]["frac_of_hbm"] == pytest.approx(k["adaln"]["gbs"] / 6800.0, abs=1e-4)
+    assert "tflops" not in k["adaln"] and "gbs" not in k["attention"]
+    assert k["gemm_fused_qkv_mlp"]["tflops"] == pytest.approx(7.83e11 / 0.43e-3 / 1e12, abs=0.1)
+    assert sum(v["share"] for v in k.values()) == pytest.approx(1.0, abs=1e-3)
+    assert bench.kernel_breakdown(recs, flops, {"adaln": 1e9}, 2, None)["adaln"]["frac_of_hbm"] is None
