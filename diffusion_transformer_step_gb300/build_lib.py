@@ -6,7 +6,10 @@ linked into diffusion_transformer_step_gb300/libdit.so.  No cmake, no torch exte
 from __future__ import annotations
 
 import concurrent.futures as cf
+import fcntl
+import json
 import os
+import platform
 import shutil
 import subprocess
 import sys
@@ -43,9 +46,34 @@ def _stale(target, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
+def _stamp(nvcc, extra_flags) -> dict:
+    """What the objects in _build were made with: another host architecture, compiler or
+    flag set makes every object stale (object files are not portable between hosts)."""
+    return {"machine": platform.machine(), "nvcc": os.path.realpath(nvcc), "flags": ARCH + FLAGS + list(extra_flags)}
+
+
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    nvcc = _nvcc()
+    """Compile what is stale and link libdit.so; returns its path.  Processes that build at
+    the same time (one per rank) take turns on a lock file, so later ones find the objects
+    fresh."""
     os.makedirs(BUILD, exist_ok=True)
+    with open(os.path.join(BUILD, "lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        try:
+            return _build_locked(force, verbose, extra_flags)
+        finally:
+            fcntl.flock(lock, fcntl.LOCK_UN)
+
+
+def _build_locked(force, verbose, extra_flags) -> str:
+    nvcc = _nvcc()
+    stamp_path = os.path.join(BUILD, "stamp.json")
+    stamp = _stamp(nvcc, extra_flags)
+    try:
+        with open(stamp_path) as f:
+            force = force or json.load(f) != stamp
+    except (OSError, ValueError):
+        force = True
     srcs = _sources()
     headers = [p for p in _deps() if not p.endswith(".cu")]
     jobs = []
@@ -74,6 +102,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{' '.join(cmd)}\n{r.stderr}")
         os.replace(LIB + ".tmp", LIB)
+    with open(stamp_path, "w") as f:
+        json.dump(stamp, f)
     return LIB
 
 
