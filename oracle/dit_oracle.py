@@ -9,7 +9,8 @@ inputs, which come from ``diffusion_transformer_step_gb300.synth``.
 Every function is the definition written out in numpy, in float64 unless the caller
 asks for float32, with no blocking, fusion or reordering beyond what the definition
 states.  Inputs are the bf16-rounded weights and activations the GPU also sees,
-upcast; no intermediate value is rounded.
+upcast; no intermediate value is rounded, except in the e4m3 variant (reading R26),
+whose quantisers take their rounding decisions on the values the GPU path feeds them.
 
 Sources, cited by page title and section:
   [card]   "flux2-klein-p100a" model card (FLUX.2 [klein] 4B on one p100a):
@@ -262,23 +263,36 @@ def _qk_norm_rope(q, k, qn, kn, cos, sin, cfg: Config):
     return apply_rope(q, cos, sin), apply_rope(k, cos, sin)
 
 
+def _project(a, w, quantised: bool, dtype, stored_bf16: bool = False):
+    """a @ w^T, or with both operands in e4m3 (linear_e4m3) when `quantised`.  `stored_bf16`
+    marks an input the GPU path holds as bf16 before its quantising pass (the attention
+    output and the SwiGLU activations, reading R18): the quantiser then sees that bf16
+    value (reading R26)."""
+    if not quantised:
+        return a @ w.astype(dtype).T
+    return linear_e4m3(bf16_round(a) if stored_bf16 else a, w, dtype)
+
+
 def dual_block(x, n_txt, w_img: StreamWeights, w_txt: StreamWeights, mod: dict, cos, sin,
-               cfg: Config, dtype=np.float64) -> np.ndarray:
+               cfg: Config, dtype=np.float64, e4m3=None) -> np.ndarray:
     """One dual-stream block over x = [B, N, H] with rows [txt | img | ref].
 
     Rows [0, n_txt) use the text weights and text modulation; every later row (target
     image and reference tokens) uses the image weights and image modulation (reading R1).
     Attention is joint over all N rows (reading R2).  Residuals are gated with the raw
-    gate vector (reading R4).
+    gate vector (reading R4).  e4m3 = "all" runs the four projections of both streams in
+    e4m3 (reading R26: the QKV and MLP-in inputs are the adaLN outputs, the out and
+    MLP-out inputs the stored attention output and activations).
     """
     H, F = cfg.hidden, cfg.mlp_hidden
+    q8 = e4m3 == "all"
     x = x.astype(dtype)
     cast = lambda a: a.astype(dtype)
     streams = [("txt", slice(0, n_txt), w_txt), ("img", slice(n_txt, x.shape[1]), w_img)]
     qs, ks, vs = [], [], []
     for name, rows, w in streams:
         y = adaln(x[:, rows], mod[f"{name}_shift_a"], mod[f"{name}_scale_a"], cfg.eps)
-        qkv = y @ cast(w.qkv).T
+        qkv = _project(y, w.qkv, q8, dtype)
         q, k, v = qkv[..., :H], qkv[..., H:2 * H], qkv[..., 2 * H:]
         q = rms_norm(_heads(q, cfg.heads, cfg.head_dim), cast(w.q_norm), cfg.eps)
         k = rms_norm(_heads(k, cfg.heads, cfg.head_dim), cast(w.k_norm), cfg.eps)
@@ -289,28 +303,31 @@ def dual_block(x, n_txt, w_img: StreamWeights, w_txt: StreamWeights, mod: dict, 
     attn = attention(q, k, v).reshape(x.shape[0], x.shape[1], H)
     out = x.copy()
     for name, rows, w in streams:
-        xs = out[:, rows] + mod[f"{name}_gate_a"] * (attn[:, rows] @ cast(w.out).T)
+        xs = out[:, rows] + mod[f"{name}_gate_a"] * _project(attn[:, rows], w.out, q8, dtype, stored_bf16=True)
         y = adaln(xs, mod[f"{name}_shift_m"], mod[f"{name}_scale_m"], cfg.eps)
-        h = y @ cast(w.mlp_in).T
+        h = _project(y, w.mlp_in, q8, dtype)
         act = swiglu(h[..., :F], h[..., F:])
-        out[:, rows] = xs + mod[f"{name}_gate_m"] * (act @ cast(w.mlp_out).T)
+        out[:, rows] = xs + mod[f"{name}_gate_m"] * _project(act, w.mlp_out, q8, dtype, stored_bf16=True)
     return out
 
 
-def single_block(x, w: SingleWeights, mod: dict, cos, sin, cfg: Config, dtype=np.float64) -> np.ndarray:
+def single_block(x, w: SingleWeights, mod: dict, cos, sin, cfg: Config, dtype=np.float64,
+                 e4m3=None) -> np.ndarray:
     """One single-stream block: one weight set over the joint sequence, attention and
-    MLP in parallel from the same modulated input (reading R8)."""
+    MLP in parallel from the same modulated input (reading R8).  e4m3 = "fused" runs the
+    fused QKV + MLP-in projection in e4m3, "all" the out-projection over [attn | act] too
+    (reading R26)."""
     H, F = cfg.hidden, cfg.mlp_hidden
     x = x.astype(dtype)
     y = adaln(x, mod["single_shift"], mod["single_scale"], cfg.eps)
-    h = y @ w.qkv_mlp.astype(dtype).T
+    h = _project(y, w.qkv_mlp, e4m3 in ("fused", "all"), dtype)
     q, k, v = h[..., :H], h[..., H:2 * H], h[..., 2 * H:3 * H]
     gate, up = h[..., 3 * H:3 * H + F], h[..., 3 * H + F:]
     q, k = _qk_norm_rope(q, k, w.q_norm.astype(dtype), w.k_norm.astype(dtype), cos, sin, cfg)
     attn = attention(q, k, _heads(v, cfg.heads, cfg.head_dim)).reshape(x.shape[0], x.shape[1], H)
     act = swiglu(gate, up)
     cat = np.concatenate([attn, act], axis=-1)
-    return x + mod["single_gate"] * (cat @ w.out.astype(dtype).T)
+    return x + mod["single_gate"] * _project(cat, w.out, e4m3 == "all", dtype, stored_bf16=True)
 
 
 def final_layer(x_img, shift, scale, w_proj, cfg: Config, dtype=np.float64) -> np.ndarray:
@@ -331,6 +348,7 @@ E4M3_MAX = 448.0
 
 def e4m3_decode(code: int) -> float:
     """The value of one e4m3 byte (NaN for the two NaN codes)."""
+    code = int(code)  # a numpy uint8 would wrap in e - 7 below
     s, e, m = (code >> 7) & 1, (code >> 3) & 15, code & 7
     if e == 15 and m == 7:
         return float("nan")
@@ -368,17 +386,72 @@ def _round_half_even(t: float) -> int:
     return f
 
 
+def _row_scales(x: np.ndarray):
+    """scale = max|row| / 448 (1 for an all-zero row) and its reciprocal, both computed in
+    fp32 as the quantiser does (reading R26)."""
+    amax = np.abs(x).max(axis=-1).astype(np.float32)
+    scale = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
+    inv = (np.float32(1.0) / scale).astype(np.float32)
+    return scale, inv
+
+
 def quantize_rows_e4m3(w: np.ndarray):
     """Per-row e4m3 quantisation as the library's weight preparation defines it, in fp32
     arithmetic: scale = max|w[r,:]| / 448 (1 for an all-zero row), q = e4m3(w * (1/scale)).
     Returns (codes uint8 [rows, cols], scale float32 [rows])."""
     w = np.asarray(w, dtype=np.float32)
-    amax = np.abs(w).max(axis=1).astype(np.float32)
-    scale = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
-    inv = (np.float32(1.0) / scale).astype(np.float32)
+    scale, inv = _row_scales(w)
     scaled = (w * inv[:, None]).astype(np.float32)
     codes = np.array([[e4m3_encode(v) for v in row] for row in scaled], dtype=np.uint8)
     return codes, scale
+
+
+def e4m3_round(x: np.ndarray) -> np.ndarray:
+    """The nearest e4m3 value of every element (ties to even, saturating to +-448), as
+    float64: the same map as e4m3_decode(e4m3_encode(.)), written per binade for whole
+    arrays.  In the binade [2^e, 2^(e+1)) (e >= -6) the grid step is 2^(e-3); below 2^-6 it
+    is the subnormal step 2^-9.  a / step is exact (a power-of-two scaling), so np.round's
+    ties-to-even is the format's."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    _, ex = np.frexp(a)  # a = m 2^ex with m in [0.5, 1): the binade starts at 2^(ex - 1)
+    step = np.where(a < 2.0 ** -6, 2.0 ** -9, np.ldexp(1.0, ex - 4))
+    q = np.minimum(np.round(a / step) * step, E4M3_MAX)
+    return np.copysign(q, x)
+
+
+def quantize_rows_e4m3_values(x: np.ndarray):
+    """Per-row e4m3 quantisation of the last axis in the kernel's precision (fp32: the
+    scale, its reciprocal and x * (1/scale) are fp32 values, reading R26).  Returns the
+    decoded e4m3 values (float64, same shape as x) and the scales (float32, x.shape[:-1]):
+    x ~ values * scale[..., None].  The same arithmetic as quantize_rows_e4m3, for whole
+    arrays."""
+    x = np.asarray(x, dtype=np.float32)
+    scale, inv = _row_scales(x)
+    return e4m3_round((x * inv[..., None]).astype(np.float32)), scale
+
+
+def bf16_round(x: np.ndarray) -> np.ndarray:
+    """Round to the nearest bfloat16 value, ties to even (finite inputs), returned as
+    float32: bf16 keeps the top 16 bits of the fp32 pattern, so the rounding adds half of
+    the dropped 16-bit field (0x8000, one less when the kept part is even) and truncates.
+    The storage rounding of the GPU path's inter-kernel tensors (reading R18); the oracle
+    applies it only where a stored value feeds a quantiser, so that both sides take the
+    quantiser's decisions on the same input (reading R26)."""
+    f = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    u = f.view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    return u.astype(np.uint32).view(np.float32).reshape(f.shape)
+
+
+def linear_e4m3(a: np.ndarray, w: np.ndarray, dtype=np.float64) -> np.ndarray:
+    """a @ w^T with both operands in e4m3 (reading R26): a quantised per token row (its
+    last axis), w [out, in] per output row, the products of the decoded values summed in
+    `dtype`, then dequantised: y[m, n] = (sum_k qa[m, k] qw[n, k]) sa[m] sw[n]."""
+    qa, sa = quantize_rows_e4m3_values(a)
+    qw, sw = quantize_rows_e4m3_values(w)
+    y = qa.astype(dtype) @ qw.astype(dtype).T
+    return y * sa[..., None].astype(dtype) * sw.astype(dtype)
 
 
 # ----------------------------------------------------------------------------------
@@ -398,11 +471,13 @@ class Weights:
 
 
 def dit_step(w: Weights, img_tokens, ref_tokens, txt_emb, sigma, ids, dtype=np.float64,
-             n_dual=None, n_single=None) -> np.ndarray:
+             n_dual=None, n_single=None, e4m3=None) -> np.ndarray:
     """One velocity evaluation ([card] task table: one DiT call per step, no CFG).
 
     img_tokens [B, n_img, C], ref_tokens [B, n_ref, C] or None, txt_emb [B, n_txt, 7680],
     sigma [B], ids [N, 4].  Returns the velocity of the target-image rows [B, n_img, C].
+    e4m3 ("fused" / "all") runs the blocks' projections in e4m3 (reading R26); the
+    embedders, the modulation and the final projection stay unquantised.
     The joint sequence is [txt | img | ref] (reading R1); reference tokens are clean
     latents, embedded by the same image embedder (reading R22).
     """
@@ -420,9 +495,10 @@ def dit_step(w: Weights, img_tokens, ref_tokens, txt_emb, sigma, ids, dtype=np.f
     nd = len(w.dual) if n_dual is None else n_dual
     ns = len(w.single) if n_single is None else n_single
     for i in range(nd):
-        x = dual_block(x, n_txt, w.dual[i][0], w.dual[i][1], mod, cos, sin, cfg, dtype)
+        x = dual_block(x, n_txt, w.dual[i][0], w.dual[i][1], mod, cos, sin, cfg, dtype,
+                       e4m3="all" if e4m3 == "all" else None)
     for i in range(ns):
-        x = single_block(x, w.single[i], mod, cos, sin, cfg, dtype)
+        x = single_block(x, w.single[i], mod, cos, sin, cfg, dtype, e4m3=e4m3)
     x_img = x[:, n_txt:n_txt + n_img]
     return final_layer(x_img, mod["final_shift"], mod["final_scale"], w.proj_out, cfg, dtype)
 

@@ -120,3 +120,37 @@ def check_fingerprints(mine: dict, kv: dict):
     for k, (s, q) in mine.items():
         ws, wq = (float(x) for x in kv[f"fingerprint.{k}"].split())
         assert abs(s - ws) <= 1e-6 * wq ** 0.5 and abs(q - wq) <= 1e-10 * wq, (k, s, ws, q, wq)
+
+
+def block_metrics(got, want, xin) -> dict:
+    """Parity figures of one block output against the oracle, all on [1, N, H] arrays.
+
+    max_abs, cos: of the whole output x_out.  The output is dominated by the unchanged
+    residual x_in, so the block's own update u = x_out - x_in is also compared: upd_cos
+    over the whole update, and the worst relative rms error of the update over any one
+    token row (row_rel) and over any one output column (col_rel).  A wrong scale of one
+    token row or one output channel (a dequantisation on the wrong index) shows there in
+    full, while it moves the whole-tensor figures by only its share of the rows or columns.
+    The oracle's output is rounded to bf16 first for the update figures, as the GPU's is."""
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    xin = np.asarray(xin, np.float64)
+    want_q = torch.from_numpy(np.asarray(want, np.float32)).to(torch.bfloat16).double().numpy()
+    du, wu = got - xin, want_q - xin
+    err = du - wu
+    rms = lambda a, ax: np.sqrt((a * a).mean(axis=ax))
+    row = rms(err, -1) / np.maximum(rms(wu, -1), 1e-30)
+    col = rms(err.reshape(-1, err.shape[-1]), 0) / np.maximum(rms(wu.reshape(-1, wu.shape[-1]), 0), 1e-30)
+    return {"max_abs": max_abs(got, want), "cos": cosine(got, want), "upd_cos": cosine(du, wu),
+            "row_rel": float(row.max()), "col_rel": float(col.max())}
+
+
+def block_metrics_fail(m: dict, bars: dict) -> list:
+    """Names of the figures of `m` outside `bars` (max_abs, row_rel, col_rel: upper
+    bounds; cos, upd_cos: lower bounds)."""
+    bad = []
+    for k, lim in bars.items():
+        v = m[k]
+        if (k in ("cos", "upd_cos") and not v >= lim) or (k not in ("cos", "upd_cos") and not v <= lim):
+            bad.append(k)
+    return bad

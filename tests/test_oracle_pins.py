@@ -549,6 +549,9 @@ def test_step_without_blocks_maps_each_target_token_to_its_own_velocity_row():
 def test_euler_loop_telescopes_and_schedule_ends_at_zero():
     sig = O.sigma_schedule(0.8, int(STRUCT["steps"]))
     assert len(sig) == 5 and sig[0] == 0.8 and sig[-1] == 0.0
+    # reading R19's interior, in closed form: equal steps of sigma_0 / 4 (no time shift)
+    np.testing.assert_allclose(sig, [0.8, 0.6, 0.4, 0.2, 0.0], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(O.sigma_schedule(1.0, 4), [1.0, 0.75, 0.5, 0.25, 0.0], rtol=0, atol=0)
     x = RNG.standard_normal((2, 3))
     v = RNG.standard_normal((2, 3))
     y = x
@@ -610,3 +613,143 @@ def test_quantize_rows_e4m3_scales_and_zero_rows():
     assert codes[0, 5] == 0xFE and codes[0, 6] == 0x30 and codes[0, 0] == 0x00
     assert (codes[1] == 0).all()                                      # all-zero row: scale 1, codes 0
     assert (codes[2] == 0x7E).all()                                   # the row maximum maps to 448
+
+
+# ---- the e4m3 variant's arithmetic (reading R26): the vectorised quantiser is pinned to
+# the scalar, definition-pinned encoder above; the quantised linear to brute force and to
+# exact cases; the blocks to the list of projections the variant names
+def _e4m3_finite_values():
+    return np.array(sorted({O.e4m3_decode(c) for c in range(256) if c not in (0x7F, 0xFF)}))
+
+
+def test_e4m3_round_matches_the_scalar_encoder_everywhere():
+    v = _e4m3_finite_values()
+    mid = 0.5 * (v[1:] + v[:-1])
+    rng = np.random.default_rng(7)
+    wide = rng.standard_normal(50000) * np.exp(rng.uniform(-14.0, 7.0, 50000))
+    xs = np.concatenate([v, mid, np.nextafter(mid, np.inf), np.nextafter(mid, -np.inf), wide,
+                         [448.0, 460.0, 464.0, 465.0, 1e30, -1e30, 2.0 ** -10, -2.0 ** -10, 0.0, -0.0]])
+    xs = xs.astype(np.float32)
+    got = O.e4m3_round(xs)
+    want = np.array([O.e4m3_decode(O.e4m3_encode(float(x))) for x in xs])
+    np.testing.assert_array_equal(got, want)
+    np.testing.assert_array_equal(np.signbit(got), np.signbit(want))     # -0 and small negatives keep the sign
+
+
+def test_quantize_rows_values_match_the_codes():
+    rng = np.random.default_rng(8)
+    x = (rng.standard_normal((40, 96)) * np.exp(rng.uniform(-6, 6, (40, 1)))).astype(np.float32)
+    x[5] = 0.0
+    x[7, 3] = 1e6
+    codes, scale = O.quantize_rows_e4m3(x)
+    vals, scale2 = O.quantize_rows_e4m3_values(x)
+    np.testing.assert_array_equal(scale2, scale)
+    np.testing.assert_array_equal(vals, np.vectorize(O.e4m3_decode)(codes))
+    # leading axes are rows too: a [2, 20, 96] array is quantised like its 40 rows
+    v3, s3 = O.quantize_rows_e4m3_values(x.reshape(2, 20, 96))
+    np.testing.assert_array_equal(v3.reshape(40, 96), vals)
+    np.testing.assert_array_equal(s3.reshape(40), scale)
+
+
+def test_bf16_round_matches_the_library_conversion_and_ties():
+    rng = np.random.default_rng(9)
+    x = (rng.standard_normal(200000) * np.exp(rng.uniform(-20, 20, 200000))).astype(np.float32)
+    lib = torch.from_numpy(x).to(torch.bfloat16).float().numpy()
+    np.testing.assert_array_equal(O.bf16_round(x), lib)
+    # ties to even: 1 + 2^-8 lies halfway between 1 and 1 + 2^-7 (kept mantissa even: 1);
+    # 1 + 3 2^-8 halfway between 1 + 2^-7 and 1 + 2^-6 (even: 1 + 2^-6); negatives mirror
+    ties = np.array([1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8, -(1 + 2.0 ** -8), -(1 + 3 * 2.0 ** -8)], np.float32)
+    np.testing.assert_array_equal(O.bf16_round(ties), [1.0, 1 + 2.0 ** -6, -1.0, -(1 + 2.0 ** -6)])
+    assert O.bf16_round(np.float32(1 + 2.0 ** -7)) == np.float32(1 + 2.0 ** -7)   # already bf16: unchanged
+
+
+def test_linear_e4m3_brute_force_and_exact_cases():
+    rng = np.random.default_rng(10)
+    a = rng.standard_normal((3, 5, 32)).astype(np.float32) * np.float32(1.7)
+    w = (rng.standard_normal((6, 32)) * 0.05).astype(np.float32)
+    got = O.linear_e4m3(a, w)
+    # brute force from the scalar, definition-pinned quantiser: sum over k of the decoded
+    # codes' products, times the token row's scale and the output row's scale
+    ca, sa = O.quantize_rows_e4m3(a.reshape(15, 32))
+    cw, sw = O.quantize_rows_e4m3(w)
+    dec = np.vectorize(O.e4m3_decode)
+    want = np.zeros((15, 6))
+    for m in range(15):
+        for n in range(6):
+            want[m, n] = sum(dec(ca[m, k]) * dec(cw[n, k]) for k in range(32)) * float(sa[m]) * float(sw[n])
+    np.testing.assert_allclose(got.reshape(15, 6), want, rtol=1e-12, atol=1e-15)
+    # rows that already lie on the grid (every element an e4m3 value times a power of two,
+    # the row maximum 448 times it) are quantised without loss: the product is exact
+    grid = _e4m3_finite_values()
+    ga = rng.choice(grid, (4, 16)); ga[:, 0] = 448.0
+    gw = rng.choice(grid, (3, 16)); gw[:, 3] = -448.0
+    ga, gw = ga * 2.0 ** -5, gw * 2.0 ** -12
+    np.testing.assert_allclose(O.linear_e4m3(ga, gw), ga @ gw.T, rtol=1e-14, atol=0)
+    # a token row's scale and an output row's scale act on their own row / column only:
+    # scaling token row 1 of a by 2^3 scales output row 1 by 2^3 exactly
+    a2 = a.reshape(15, 32).copy(); a2[1] *= 8.0
+    g2 = O.linear_e4m3(a2, w)
+    np.testing.assert_array_equal(g2[1], 8.0 * got.reshape(15, 6)[1])
+    np.testing.assert_array_equal(np.delete(g2, 1, 0), np.delete(got.reshape(15, 6), 1, 0))
+    w2 = w.copy(); w2[4] *= 0.25
+    g3 = O.linear_e4m3(a, w2)
+    np.testing.assert_array_equal(g3[..., 4], 0.25 * got[..., 4])
+    np.testing.assert_array_equal(np.delete(g3, 4, -1), np.delete(got, 4, -1))
+
+
+def _recording_quantiser(monkeypatch, identity=False):
+    """Replace the per-row quantiser by a recorder of its inputs (identity=True: also
+    pass the input through unquantised, with unit scales)."""
+    seen = []
+    real = O.quantize_rows_e4m3_values
+
+    def rec(x):
+        x32 = np.asarray(x, np.float32)
+        seen.append((x32.shape, bool((O.bf16_round(x32) == x32).all())))
+        if identity:
+            return np.asarray(x, np.float64), np.ones(x32.shape[:-1], np.float32)
+        return real(x)
+
+    monkeypatch.setattr(O, "quantize_rows_e4m3_values", rec)
+    return seen
+
+
+def test_e4m3_blocks_quantise_the_projections_the_variant_names(monkeypatch):
+    cfg, wl, wi, wt, ws, x, m, c, s = _tiny_block_setup()
+    H, F, N = cfg.hidden, cfg.mlp_hidden, x.shape[1]
+    nt, ni = wl.n_txt, N - wl.n_txt
+    mod = O.split_modulation(m, H)
+    # with the quantiser replaced by the identity (and every stored value already bf16,
+    # which the identity path cannot see), the e4m3 blocks are the plain blocks: the variant
+    # changes nothing but the quantised projections
+    seen = _recording_quantiser(monkeypatch, identity=True)
+    monkeypatch.setattr(O, "bf16_round", lambda a: np.asarray(a))
+    np.testing.assert_allclose(O.dual_block(x, nt, wi, wt, mod, c, s, cfg, e4m3="all"),
+                               O.dual_block(x, nt, wi, wt, mod, c, s, cfg), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(O.single_block(x, ws, mod, c, s, cfg, e4m3="all"),
+                               O.single_block(x, ws, mod, c, s, cfg), rtol=0, atol=1e-12)
+    monkeypatch.undo()
+    # which operands are quantised, in order, and which ones the quantiser reads as stored
+    # bf16 values (the attention output and the activations, reading R18) or unrounded
+    # (the adaLN outputs, which the GPU quantises straight from fp32)
+    seen = _recording_quantiser(monkeypatch)
+    O.dual_block(x, nt, wi, wt, mod, c, s, cfg, e4m3="all")
+    shapes = [sh for sh, _ in seen]
+    per_stream = lambda n: [(1, n, H), (3 * H, H)]
+    assert shapes == (per_stream(nt) + per_stream(ni) +                       # QKV: txt, img
+                      [(1, nt, H), (H, H), (1, nt, H), (2 * F, H), (1, nt, F), (H, F)] +   # txt: out, MLP-in, MLP-out
+                      [(1, ni, H), (H, H), (1, ni, H), (2 * F, H), (1, ni, F), (H, F)]), shapes
+    stored = [b for (sh, b), i in zip(seen, range(len(seen))) if i % 2 == 0]   # activations only
+    assert stored == [False, False, True, False, True, True, False, True], stored
+    seen.clear()
+    O.single_block(x, ws, mod, c, s, cfg, e4m3="fused")
+    assert [sh for sh, _ in seen] == [(1, N, H), (3 * H + 2 * F, H)] and not seen[0][1]
+    seen.clear()
+    O.single_block(x, ws, mod, c, s, cfg, e4m3="all")
+    assert [sh for sh, _ in seen] == [(1, N, H), (3 * H + 2 * F, H), (1, N, H + F), (H, H + F)]
+    assert seen[2][1] and not seen[0][1]
+    # and e4m3=None quantises nothing
+    seen.clear()
+    O.dual_block(x, nt, wi, wt, mod, c, s, cfg)
+    O.single_block(x, ws, mod, c, s, cfg)
+    assert seen == []
