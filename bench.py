@@ -16,11 +16,19 @@ tokens, batch 1).  Prints ONE JSON line on rank 0.
              records CUDA events around every launch and also gives the per-class `kernels`
              breakdown): its algorithmic FLOPs per launch / its mean launch time, measured
              live in the timed region with CUDA events recorded around that class's launches
-             only, on their own stream
+             only, on their own stream; `peak` is the measured bf16 burst figure (the timed
+             region lasts well under a second), with the sustained figure and the dense
+             peak at the run's own median SM clock beside it
   fp8_variant  the same step with every block projection in e4m3 (not the headline)
   cpu_baseline  the CPU oracle (fp32 numpy) timed on a bounded sample (one dual-stream and
-             one single-stream block at the same shape), scaled to the 5 + 20 blocks
-  --impl reference  times the CPU oracle as the reference arm (rank 0 only).
+             one single-stream block at the same shape); the line gives both measured block
+             times and the scaling to the step's 5 + 20 blocks
+  --impl reference  times the CPU oracle as the reference arm (rank 0 only): every step is
+             the same bounded sample, `ms_per_step` the sample's measured time, `value`
+             steps/s scaled from it as above.
+  --gpus N   N replicas, one process per GPU, each on its own batch rows (no collective on
+             the data path); without WORLD_SIZE in the environment the script starts them
+             itself under torch.distributed.run.
 
 Weights are seeded random (no trained checkpoint exists here); the step streams 7.4 GB
 of weights per step, far larger than the 129 MB L2, so no L2 flush is needed between
@@ -48,6 +56,10 @@ UNIT = "steps/s"
 # MEASURED_PEAKS.json when that file is present, else these fallback figures (one earlier
 # GB300 measurement), reported as such.
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# Dense bf16 tensor rate of one SM: one M128 N256 K16 tcgen05.mma (2*128*256*16 FLOP) per
+# 128 cycles, as measured on sm_103a with one issuing thread per SM (design notes, section 5).
+# x the SM count x the SM clock gives the dense peak at a given clock.
+BF16_FLOP_PER_CLK_PER_SM = 8192.0
 
 # DRAM traffic per launch of the dominant kernel from one ncu capture (see profiles/);
 # None until captured for the current kernel.
@@ -136,6 +148,16 @@ def step_flops(wd, batch, n_txt, n_img, n_ref):
     return batch * ((wd.n_dual + wd.n_single) * blk + embed)
 
 
+def dense_peak_at_clock(sm_mhz, props):
+    """Dense bf16 peak (TFLOP/s) of this GPU at the median SM clock seen during the timed
+    region: SMs x BF16_FLOP_PER_CLK_PER_SM x clock.  None without a clock sample."""
+    if not sm_mhz:
+        return None
+    sms = int(props.multi_processor_count)
+    return {"tflops": round(sms * BF16_FLOP_PER_CLK_PER_SM * float(sm_mhz) * 1e6 / 1e12, 1), "sms": sms,
+            "sm_mhz": float(sm_mhz), "flop_per_clk_per_sm": BF16_FLOP_PER_CLK_PER_SM}
+
+
 # ---------------------------------------------------------------------------------- clocks
 class ClockSampler:
     """nvidia-smi samples (every 200 ms) of SM clock and throttle reasons while running."""
@@ -221,6 +243,26 @@ def reduce_max(x: float, world: int, device) -> float:
     return float(t.item())
 
 
+def free_port() -> int:
+    import socket
+    with socket.socket() as so:
+        so.bind(("127.0.0.1", 0))
+        return so.getsockname()[1]
+
+
+def replica_command(n: int, script: str, argv, port: int):
+    """The command that runs `script argv` as n ranks of one node under torch.distributed.run,
+    rendezvous on 127.0.0.1."""
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+            "--master-addr", "127.0.0.1", "--master-port", str(port), script, *argv]
+
+
+def relaunch_as_replicas(n: int, script: str, argv) -> int:
+    """Start n replicas of this bench (one process per GPU, RANK / LOCAL_RANK / WORLD_SIZE
+    set by torch.distributed.run) and return their exit status.  Rank 0 prints the line."""
+    return subprocess.call(replica_command(n, script, argv, free_port()))
+
+
 def whole_job_steps_per_s(ms_per_step_max: float, world: int) -> float:
     """Every rank runs its own replica (its own batch rows): the job completes `world`
     steps in the slowest rank's step time."""
@@ -228,10 +270,11 @@ def whole_job_steps_per_s(ms_per_step_max: float, world: int) -> float:
 
 
 # ---------------------------------------------------------------------------------- CPU oracle
-def oracle_block_times(wl, seed=0, reps=1):
-    """Seconds of one dual-stream and one single-stream block of the fp32 oracle at wl's shape."""
+def oracle_blocks(wl, seed=0):
+    """Set up one dual-stream and one single-stream block of the fp32 oracle at wl's shape
+    (seeded weights and inputs); returns a function that runs both once and returns the
+    seconds each took."""
     import numpy as np
-    import torch
     from diffusion_transformer_step_gb300 import synth
     from oracle import dit_oracle as O
 
@@ -246,14 +289,33 @@ def oracle_block_times(wl, seed=0, reps=1):
     c, s = c.astype(np.float32), s.astype(np.float32)
     x, m = f(bi["x"]), O.split_modulation(f(bi["mod"]), wd.hidden)
     wi, wt, ws = sw(img), sw(txt), O.SingleWeights(**{k: f(v) for k, v in sgl.items()})
-    t0 = time.perf_counter()
-    for _ in range(reps):
+
+    def run():
+        t0 = time.perf_counter()
         O.dual_block(x, wl.n_txt, wi, wt, m, c, s, cfg, np.float32)
-    t1 = time.perf_counter()
-    for _ in range(reps):
+        t1 = time.perf_counter()
         O.single_block(x, ws, m, c, s, cfg, np.float32)
-    t2 = time.perf_counter()
-    return (t1 - t0) / reps, (t2 - t1) / reps
+        t2 = time.perf_counter()
+        return t1 - t0, t2 - t1
+
+    return run
+
+
+def oracle_sample(wl, reps=1):
+    """The bounded CPU sample both CPU legs time: one dual-stream and one single-stream block
+    of the fp32 oracle at wl's shape.  Returns the measured seconds of each and the full
+    step's seconds scaled from them (n_dual dual + n_single single blocks; the embedders,
+    the modulation and the final layer are under 0.1 % of the step's FLOPs)."""
+    run = oracle_blocks(wl)
+    td = ts = 0.0
+    for _ in range(reps):
+        a, b = run()
+        td, ts = td + a / reps, ts + b / reps
+    wd = wl.widths
+    return {"dual_block_s": td, "single_block_s": ts, "sample_s": td + ts,
+            "step_s_scaled": wd.n_dual * td + wd.n_single * ts,
+            "scaled_to": f"{wd.n_dual} dual + {wd.n_single} single blocks: step_s = {wd.n_dual} t_dual + "
+                         f"{wd.n_single} t_single"}
 
 
 def cpu_cores():
@@ -265,38 +327,37 @@ def cpu_cores():
 
 # ---------------------------------------------------------------------------------- arms
 def run_reference(args, wl):
-    """The CPU oracle as the reference arm: each step is a bounded sample (one single-stream
-    block of the same shape, fp32), scaled to the step's 25 blocks."""
+    """The CPU oracle as the reference arm.  Every step is the same bounded sample (one
+    dual-stream and one single-stream block of the workload's shape, fp32 numpy); the line's
+    ms_per_step is the sample's measured time per step, and value is the workload's steps/s
+    scaled from the two measured block times (oracle_sample)."""
     from oracle import dit_oracle as O  # noqa: F401  (the one other place bench runs the oracle)
-    import numpy as np
-    import torch
-    from diffusion_transformer_step_gb300 import synth
-    from oracle import dit_oracle as Ox
 
     wd = wl.widths
-    g = synth.generator(0)
-    sgl = synth.single_weights(wd, g)
-    bi = synth.block_inputs(synth.Workload("b1", wd, 1, wl.n_txt, wl.grid, wl.ref_grids), 0)
-    f = lambda t: t.float().numpy()
-    cfg = Ox.Config(hidden=wd.hidden, heads=wd.heads, head_dim=wd.head_dim, mlp_hidden=wd.mlp_hidden)
-    c, s = Ox.rope_table(Ox.token_ids(wl.n_txt, *wl.grid, wl.ref_grids))
-    c, s = c.astype(np.float32), s.astype(np.float32)
-    x, m = f(bi["x"]), Ox.split_modulation(f(bi["mod"]), wd.hidden)
-    ws = Ox.SingleWeights(**{k: f(v) for k, v in sgl.items()})
+    run = oracle_blocks(wl)
     for _ in range(args.warmup):
-        Ox.single_block(x, ws, m, c, s, cfg, np.float32)
+        run()
     t0 = time.perf_counter()
+    tds, tss = [], []
     for _ in range(args.steps):
-        Ox.single_block(x, ws, m, c, s, cfg, np.float32)
-    dt = (time.perf_counter() - t0) / args.steps
-    step_s = dt * (wd.n_dual + wd.n_single)
+        td, ts = run()
+        tds.append(td)
+        tss.append(ts)
+    wall = time.perf_counter() - t0
+    td, ts = statistics.mean(tds), statistics.mean(tss)
+    step_s = wd.n_dual * td + wd.n_single * ts
     value = wl.batch / step_s
     flops = step_flops(wd, wl.batch, wl.n_txt, wl.n_img, wl.n_ref)
-    sample = f"one single-stream block of the {wl.name} shape per step (fp32 numpy oracle), x{wd.n_dual + wd.n_single} blocks"
+    sample = (f"per step one dual-stream ({td:.2f} s) and one single-stream ({ts:.2f} s) block of the {wl.name} "
+              f"shape, fp32 numpy oracle; value scaled to {wd.n_dual} dual + {wd.n_single} single blocks")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": wall / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": workload_config(wl), "tflops": flops / step_s / 1e12,
+            "sample": {"what": "one dual-stream + one single-stream block per step (ms_per_step is its measured "
+                               "time)", "dual_block_s": td, "single_block_s": ts,
+                       "step_s_scaled": step_s,
+                       "scaled_to": f"{wd.n_dual} t_dual + {wd.n_single} t_single"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -465,23 +526,31 @@ def run_ours(args, wl, rank, world, local_rank):
     dom_ms = [t for name, t in records if name == dom]
     mean_ms = sum(dom_ms) / len(dom_ms)
     achieved = flops_cls[dom] / (mean_ms / 1e3) / 1e12
-    peak = peak_get(peaks, "bf16_tflops_sustained", "bf16_tflops")
+    peak = peak_get(peaks, "bf16_tflops", "bf16_tflops_sustained")
+    peak_sus = peak_get(peaks, "bf16_tflops_sustained")
+    clock_peak = dense_peak_at_clock(clocks.get("sm_mhz"), torch.cuda.get_device_properties(local_rank))
     tr = NCU_TRAFFIC.get(dom)
     roofline = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
-                "frac": round(achieved / peak, 4), "peak_source": f"bf16 sustained, of {src}",
+                "frac": round(achieved / peak, 4), "peak_source": f"bf16 burst, of {src}",
                 "traffic": tr, "flops_per_launch": flops_cls[dom], "launch_ms_mean": round(mean_ms, 4),
-                "frac_of_nominal_2250": round(achieved / 2250.0, 4)}
+                "frac_of_sustained": round(achieved / peak_sus, 4) if peak_sus else None,
+                "clock_scaled_peak": clock_peak,
+                "frac_of_clock_scaled_peak": round(achieved / clock_peak["tflops"], 4) if clock_peak else None}
+    if roofline["frac"] > 1.0:
+        roofline["note"] = "frac above 1: the denominator (a cuBLAS burst) ran at a lower clock than this kernel"
     flops = step_flops(wd, wl.batch, wl.n_txt, wl.n_img, wl.n_ref)
     tflops = flops / (ms_step / 1e3) / 1e12
 
     # ---- CPU oracle baseline on a bounded sample
     cpu = None
     if not args.no_cpu_baseline:
-        td, ts = oracle_block_times(wl)
-        step_s = wd.n_dual * td + wd.n_single * ts
-        cpu = {"value": wl.batch / step_s / wl.batch, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-               "sample": f"one dual-stream ({td:.2f} s) and one single-stream ({ts:.2f} s) block of the "
-                         f"{wl.name} shape, fp32 numpy oracle, scaled to {wd.n_dual}+{wd.n_single} blocks"}
+        smp = oracle_sample(wl)
+        cpu = {"value": wl.batch / smp["step_s_scaled"], "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"one dual-stream ({smp['dual_block_s']:.2f} s) and one single-stream "
+                         f"({smp['single_block_s']:.2f} s) block of the {wl.name} shape, fp32 numpy oracle, "
+                         f"measured once; value scaled to {smp['scaled_to']}",
+               "dual_block_s": round(smp["dual_block_s"], 3), "single_block_s": round(smp["single_block_s"], 3),
+               "step_s_scaled": round(smp["step_s_scaled"], 2)}
 
     line = {"metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
@@ -489,8 +558,9 @@ def run_ours(args, wl, rank, world, local_rank):
             "config": workload_config(wl),
             "tflops": round(tflops, 1),
             "frac_of_bf16_peak": {"measured_or_fallback": src,
-                                  "burst": round(tflops / peak_get(peaks, "bf16_tflops", "bf16_tflops_sustained"), 4),
-                                  "sustained": round(tflops / peak, 4), "nominal_2250": round(tflops / 2250.0, 4)},
+                                  "burst": round(tflops / peak, 4),
+                                  "sustained": round(tflops / peak_sus, 4) if peak_sus else None,
+                                  "clock_scaled": round(tflops / clock_peak["tflops"], 4) if clock_peak else None},
             "roofline": roofline, "kernels": kernels,
             "kernels_source": f"untimed pass of {bd_steps} steps with an event pair around every launch; the "
                               f"timed region records events around the {dom} launches only",
@@ -524,9 +594,15 @@ def main():
     from diffusion_transformer_step_gb300 import synth
     wl = synth.WORKLOADS[args.workload]
 
+    if args.gpus < 1:
+        raise SystemExit("--gpus must be >= 1")
+    if args.impl == "ours" and args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(relaunch_as_replicas(args.gpus, os.path.abspath(__file__), sys.argv[1:]))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "ours" and world != args.gpus:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE {world}: launch one process per GPU")
     if args.impl == "reference":
         if rank == 0:
             run_reference(args, wl)

@@ -116,3 +116,77 @@ def test_stalled_replica_times_out_the_next_collective_of_the_others():
     print(f"waiting rank: {what} after {seconds:.2f} s")
     assert what != "returned"
     assert 2.0 <= seconds < 8.0          # the group's 3 s timeout, not the stalled peer's exit
+
+
+def test_bench_gpus_n_starts_n_replicas_itself(monkeypatch):
+    """`python bench.py --gpus 2` outside any launcher re-runs itself as 2 ranks under
+    torch.distributed.run (rendezvous on 127.0.0.1), passing its own arguments on."""
+    import sys
+    import bench
+    seen = {}
+
+    def fake(n, script, argv):
+        seen.update(n=n, script=script, argv=list(argv))
+        return 0
+
+    monkeypatch.setattr(bench, "relaunch_as_replicas", fake)
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--gpus", "2", "--steps", "3", "--warmup", "3"])
+    with pytest.raises(SystemExit) as e:
+        bench.main()
+    assert e.value.code == 0
+    assert seen["n"] == 2 and seen["script"].endswith("bench.py")
+    assert seen["argv"] == ["--gpus", "2", "--steps", "3", "--warmup", "3"]
+    cmd = bench.replica_command(2, "/x/bench.py", ["--gpus", "2"], 29500)
+    assert cmd[1:4] == ["-m", "torch.distributed.run", "--nnodes=1"] and "--nproc-per-node=2" in cmd
+    assert cmd[cmd.index("--master-addr") + 1] == "127.0.0.1" and cmd[-3:] == ["/x/bench.py", "--gpus", "2"]
+    # under a launcher, WORLD_SIZE must agree with --gpus
+    monkeypatch.setenv("WORLD_SIZE", "4")
+    with pytest.raises(SystemExit) as e:
+        bench.main()
+    assert "WORLD_SIZE 4" in str(e.value.code)
+
+
+STANDIN = r'''
+import json, os, sys, time
+sys.path.insert(0, os.environ["BENCH_ROOT"])
+import bench
+if "WORLD_SIZE" not in os.environ:
+    sys.exit(bench.relaunch_as_replicas(2, os.path.abspath(__file__), []))
+bench.init_replica_group("gloo", timeout_s=60.0)
+import torch.distributed as dist
+rank, world = dist.get_rank(), dist.get_world_size()
+dist.barrier()
+t0 = time.perf_counter()
+for _ in range(3):
+    time.sleep(0.02 * (rank + 1))          # the stand-in step: rank 1 is the slow replica
+ms = (time.perf_counter() - t0) / 3 * 1e3
+m = bench.reduce_max(ms, world, "cpu")
+if rank == 0:
+    print(json.dumps({"n_gpus": world, "ms_per_step": m, "value": bench.whole_job_steps_per_s(m, world),
+                      "rank0_ms": ms}), flush=True)
+dist.barrier()
+dist.destroy_process_group()
+'''
+
+
+def test_replica_launcher_brings_up_two_gloo_ranks(tmp_path):
+    """The launcher bench.py uses, run for real with a CPU stand-in step: two ranks come
+    up, join one gloo group, and rank 0 alone prints n_gpus 2 and the whole-job rate of
+    the slowest rank."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    script = tmp_path / "standin.py"
+    script.write_text(STANDIN)
+    env = dict(os.environ, BENCH_ROOT=root, OMP_NUM_THREADS="1")
+    env.pop("WORLD_SIZE", None)
+    r = subprocess.run([sys.executable, str(script)], capture_output=True, text=True, timeout=300, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [json.loads(ln) for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = lines[0]
+    assert d["n_gpus"] == 2
+    assert d["ms_per_step"] >= 40.0 and d["ms_per_step"] > d["rank0_ms"]      # the slower rank's time
+    assert abs(d["value"] - 2 / (d["ms_per_step"] / 1e3)) < 1e-9
