@@ -18,6 +18,11 @@ namespace dit {
 // ---------------------------------------------------------------------------------
 namespace {
 std::atomic<unsigned long long> g_launches{0};
+// While this thread captures a step into a graph, its launches do not run: they are
+// counted here instead and added to g_launches each time the graph is replayed.  Per
+// thread, so that launches other threads issue meanwhile are counted as usual.
+thread_local bool t_capturing = false;
+thread_local unsigned long long t_captured = 0;
 std::mutex g_timing_mu;
 bool g_timing_on = false;
 unsigned int g_timing_mask = ~0u;  // classes whose launches get an event pair
@@ -39,7 +44,10 @@ const char* kernel_class_name(int cls) {
 }
 
 LaunchScope::LaunchScope(int cls, cudaStream_t stream) : slot_(-1), stream_(stream) {
-  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (t_capturing)
+    ++t_captured;
+  else
+    g_launches.fetch_add(1, std::memory_order_relaxed);
   std::lock_guard<std::mutex> lk(g_timing_mu);
   if (g_timing_on && ((g_timing_mask >> cls) & 1u) && g_rec_used < (int)g_recs.size()) {
     slot_ = g_rec_used++;
@@ -805,15 +813,16 @@ dit_status dit_step_graph_create(const dit_weights* w, const dit_shape* shape, c
   DIT_CUDA(cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking));
   cudaGraph_t g = nullptr;
   cudaError_t ce = cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal);
-  const unsigned long long before = g_launches.load();
   dit_status es = DIT_OK;
+  // Captured launches do not run: count them when the graph is replayed instead.
+  t_capturing = true;
+  t_captured = 0;
   if (ce == cudaSuccess) {
     es = enqueue((dit_stream_t)cap);
     ce = cudaStreamEndCapture(cap, &g);
   }
-  // Captured launches did not run: count them when the graph is replayed instead.
-  const unsigned long long kernels = g_launches.load() - before;
-  g_launches.fetch_sub(kernels);
+  t_capturing = false;
+  const unsigned long long kernels = t_captured;
   cudaStreamDestroy(cap);
   if (es != DIT_OK || ce != cudaSuccess) {
     if (g) cudaGraphDestroy(g);

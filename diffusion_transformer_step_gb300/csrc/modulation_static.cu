@@ -46,7 +46,12 @@ cudaError_t static_scratch(float** out) {
   if (g_static_addr[dev] == nullptr) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_static_scratch);
-    if (e != cudaSuccess) return e;
+    if (e != cudaSuccess) {
+      // Clear the runtime's last-error slot so that a later, unrelated call does not report
+      // this failure as its own (a lookup refused during a stream capture, for example).
+      (void)cudaGetLastError();
+      return e;
+    }
     g_static_addr[dev] = static_cast<float*>(p);
   }
   *out = g_static_addr[dev];

@@ -33,8 +33,10 @@
  *     writes a status word in the workspace and the kernel unwinds; dit_sync_status()
  *     reports it as DIT_ERR_TIMEOUT.
  *   - No C++ exception crosses this boundary.  Calls on different workspaces and
- *     streams may run concurrently from different host threads, except the timing
- *     functions (dit_timing_*), which use process-wide state.
+ *     streams may run concurrently from different host threads, with two exceptions,
+ *     both process-wide state: the timing functions (dit_timing_*), and
+ *     dit_modulation_static, whose calls all share one fixed device array (two of its
+ *     calls that overlap on the GPU race on it).
  */
 #ifndef DIT_H_
 #define DIT_H_
@@ -206,8 +208,12 @@ dit_status dit_modulation(const dit_weights* w, const float* sigma_dev, int batc
                           size_t ws_bytes, dit_stream_t stream);
 
 /* One dual-stream block `layer` (0 <= layer < n_dual), in place on x_dev [B, N, H]
- * (rows text | image | reference).  Per stream s (text rows use `txt`, image and
- * reference rows use `img` weights and modulation):
+ * (rows text | image | reference).  Sources: "tt_flux2_klein -- Python reference",
+ * Modules (tt_dit.py: the 5 dual-stream blocks, each with its own text and image weights)
+ * and "Things that are easy to get wrong" (the joint sequence and RoPE); "flux2-klein-p100a"
+ * Caveats (all 512 padded text rows, no mask; modulation global per step).  The block maths
+ * is not written on the pages: the form below is the library's reading.  Per stream s
+ * (text rows use `txt`, image and reference rows use `img` weights and modulation):
  *   y = (1 + scale_a) LN(x) + shift_a;  q, k, v = y qkv^T;  q, k <- RMSNorm_head * w;
  *   q, k <- RoPE;  o = joint softmax attention over all N rows, no mask;
  *   x += gate_a (o out^T);  y = (1 + scale_m) LN(x) + shift_m;
@@ -217,7 +223,11 @@ dit_status dit_dual_block_fwd(const dit_weights* w, int layer, const dit_shape* 
                               const void* mod_dev, const float* rope_dev, void* ws, size_t ws_bytes,
                               dit_stream_t stream);
 
-/* One single-stream block `layer` (0 <= layer < n_single), in place on x_dev [B, N, H]:
+/* One single-stream block `layer` (0 <= layer < n_single), in place on x_dev [B, N, H].
+ * Sources: "tt_flux2_klein -- Python reference", Modules (tt_dit.py: the 20 single-stream
+ * blocks, one weight set over the joint sequence) and "Things that are easy to get wrong";
+ * "flux2-klein-p100a" Caveats (modulation global per step).  The fused projection's column
+ * order is the library's reading:
  *   y = (1 + scale) LN(x) + shift;  [q | k | v | gate | up] = y qkv_mlp^T;
  *   q, k <- RMSNorm_head * w, RoPE;  o = attention;  act = silu(gate) * up;
  *   x += gate_s ([o | act] out^T).  Other arguments as dit_dual_block_fwd. */
@@ -225,7 +235,10 @@ dit_status dit_single_block_fwd(const dit_weights* w, int layer, const dit_shape
                                 const void* mod_dev, const float* rope_dev, void* ws, size_t ws_bytes,
                                 dit_stream_t stream);
 
-/* One whole DiT step (one velocity evaluation): modulation from sigma, embedders
+/* One whole DiT step (one velocity evaluation; "flux2-klein-p100a" task table: each of the
+ * 4 steps is one DiT call, guidance 1.0, no CFG; "tt_flux2_klein -- Python reference",
+ * Lower-level entry points: denoise consumes encode()'s [512, 7680] text features and the
+ * reference tokens; Modules: tt_dit.py): modulation from sigma, embedders
  * (img/ref tokens by x_emb, text by ctx_emb) into the joint stream, n_dual dual blocks,
  * n_single single blocks, then the final layer (1 + scale_f) LN(x) + shift_f and
  * proj_out on the target-image rows only.
