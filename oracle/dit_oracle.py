@@ -407,23 +407,34 @@ def quantize_rows_e4m3(w: np.ndarray):
 
 
 def e4m3_round(x: np.ndarray) -> np.ndarray:
-    """The nearest e4m3 value of every element (ties to even, saturating to +-448), as
-    float64: the same map as e4m3_decode(e4m3_encode(.)), written per binade for whole
-    arrays.  In the binade [2^e, 2^(e+1)) (e >= -6) the grid step is 2^(e-3); below 2^-6 it
-    is the subnormal step 2^-9.  a / step is exact (a power-of-two scaling), so np.round's
-    ties-to-even is the format's."""
-    x = np.asarray(x, dtype=np.float64)
-    a = np.abs(x)
-    _, ex = np.frexp(a)  # a = m 2^ex with m in [0.5, 1): the binade starts at 2^(ex - 1)
-    step = np.where(a < 2.0 ** -6, 2.0 ** -9, np.ldexp(1.0, ex - 4))
-    q = np.minimum(np.round(a / step) * step, E4M3_MAX)
-    return np.copysign(q, x)
+    """The nearest e4m3 value of every element of a float32 array (ties to even,
+    saturating to +-448), as float32 (every e4m3 value is exact in float32): the same map
+    as e4m3_decode(e4m3_encode(.)), for whole arrays.  Magnitudes are first clipped to 448,
+    the largest finite value.  From 2^-6 up, e4m3 keeps 3 significand bits, so the float32
+    value is rounded to the top 3 of its 23 stored significand bits: add half of the 20
+    dropped bits' weight (0x80000, one less when the lowest kept bit is even) and clear
+    them; a carry out of the significand moves to the next binade, as it should.  Below
+    2^-6 the grid is the subnormal step 2^-9: x * 2^9 rounded to an integer (exact
+    scaling, rint is ties-to-even)."""
+    x = np.asarray(x, dtype=np.float32)
+    a = np.minimum(np.abs(x), np.float32(E4M3_MAX))
+    u = a.view(np.uint32)
+    t = np.right_shift(u, np.uint32(20))
+    np.bitwise_and(t, np.uint32(1), out=t)
+    t += np.uint32(0x7FFFF)
+    t += u
+    np.bitwise_and(t, np.uint32(0xFFF00000), out=t)
+    q = t.view(np.float32)
+    small = a < np.float32(2.0 ** -6)
+    if small.any():
+        q[small] = np.rint(a[small] * np.float32(512.0)) * np.float32(1.0 / 512.0)
+    return np.copysign(q, x, out=q)
 
 
 def quantize_rows_e4m3_values(x: np.ndarray):
     """Per-row e4m3 quantisation of the last axis in the kernel's precision (fp32: the
     scale, its reciprocal and x * (1/scale) are fp32 values, reading R26).  Returns the
-    decoded e4m3 values (float64, same shape as x) and the scales (float32, x.shape[:-1]):
+    decoded e4m3 values (float32, exact; same shape as x) and the scales (float32, x.shape[:-1]):
     x ~ values * scale[..., None].  The same arithmetic as quantize_rows_e4m3, for whole
     arrays."""
     x = np.asarray(x, dtype=np.float32)

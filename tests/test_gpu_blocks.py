@@ -2,6 +2,10 @@
 
 Acceptance: per block output max-abs <= 3e-2 and cosine >= 0.999 (bf16 GPU path against
 the unrounded oracle on the same bf16 inputs); the full 25-block step cosine >= 0.995.
+The block's own update and, at klein width, its worst token row and output column are
+checked too (bars and their derivation in helpers.py).  The e4m3 variant is checked
+against the oracle's e4m3 path (the same quantisation, reading R26) with bars derived
+from the arithmetic, and against the unquantised oracle as an accuracy report.
 Batch rows are independent ("FLUX.2 [klein] 4B/9B + Z-Image-Turbo on a shared DiT
 scaffold": rows independent of their batch neighbours bit for bit), so at batch 4 the
 oracle checks rows 0 and 3 and the GPU's own batch invariance covers the rest.
@@ -19,14 +23,7 @@ import helpers as Hx
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
-BLOCK_ATOL, BLOCK_COS, STEP_COS = 3e-2, 0.999, 0.995
-# e4m3 keeps 3 mantissa bits (relative rounding up to 2^-4, rms 2^-4/sqrt(3) per operand):
-# each product of two quantised operands carries ~5 % rms relative error, so the
-# projections' outputs do too.  Measured on GB300 with every block projection in e4m3:
-# 1024^2 single and dual blocks max-abs 0.139, update-cosine 0.9977; tiny blocks
-# update-cosine 0.977-0.979 (their small updates are also quantised by the bf16 output);
-# full 1024^2 step cosine 0.990.  Bars at about twice those errors; bf16 keeps 3e-2.
-FP8_BLOCK_ATOL, FP8_UPDATE_COS, FP8_STEP_COS = 0.25, 0.97, 0.98
+STEP_COS = 0.995
 
 TINY_REF = synth.Workload("tiny_ref_b2", synth.TINY, 2, 40, (7, 20), ((6, 10),))       # N = 240, ragged
 TINY_MULTI = synth.Workload("tiny_3ref", synth.TINY, 1, 24, (4, 6), ((2, 3), (3, 3), (1, 5)))
@@ -57,6 +54,13 @@ def _status(dit, ws):
     assert st == dit.DIT_OK, f"device wait gave up at site {where:#x}"
 
 
+def _check(tag, got, want, xin, bars, rowcol=None):
+    m = Hx.block_metrics(got, want, xin)
+    print(f"{tag}: " + " ".join(f"{k} {v:.5g}" for k, v in m.items()))
+    bad = Hx.block_metrics_fail(m, {**bars, **(rowcol or {})})
+    assert not bad, (tag, bad, m)
+
+
 def run_block(dit, kind, wl, seed=0, check_rows=None, fp8=False):
     wd = wl.widths
     g = synth.generator(seed)
@@ -81,26 +85,27 @@ def run_block(dit, kind, wl, seed=0, check_rows=None, fp8=False):
     c, s = c.astype(dt), s.astype(dt)
     xin, m = Hx.to_np(bi["x"], dt), Hx.to_np(bi["mod"], dt)
     rows = range(wl.batch) if check_rows is None else check_rows
-    for b in rows:
+    e4m3 = {False: None, True: "all", "all": "all", "fused": "fused"}[fp8]
+
+    def oracle(b, q):
         mod_b = O.split_modulation(m[b:b + 1], wd.hidden)
         if kind == "dual":
             img, txt = logical["dual"][0]
-            want = O.dual_block(xin[b:b + 1], wl.n_txt, Hx.oracle_stream(img, dt), Hx.oracle_stream(txt, dt), mod_b,
-                                c, s, cfg, dt)
+            return O.dual_block(xin[b:b + 1], wl.n_txt, Hx.oracle_stream(img, dt), Hx.oracle_stream(txt, dt), mod_b,
+                                c, s, cfg, dt, e4m3=q)
+        return O.single_block(xin[b:b + 1], Hx.oracle_single(logical["single"][0], dt), mod_b, c, s, cfg, dt,
+                              e4m3=q)
+
+    for b in rows:
+        tag = f"{kind} {wl.name} row {b}"
+        if e4m3 is None:
+            _check(tag, got[b:b + 1], oracle(b, None), xin[b:b + 1], Hx.BF16_BARS, Hx.BF16_ROWCOL_BARS if big else None)
         else:
-            want = O.single_block(xin[b:b + 1], Hx.oracle_single(logical["single"][0], dt), mod_b, c, s, cfg, dt)
-        err, cs = Hx.max_abs(got[b:b + 1], want), Hx.cosine(got[b:b + 1], want)
-        # The cosine above is dominated by the unchanged residual x; also check the block's
-        # own update x_out - x_in.  Its GPU value is quantised by the bf16 output, so it is
-        # compared with the oracle's output rounded to bf16 the same way.
-        want_q = torch.from_numpy(np.asarray(want, np.float32)).to(torch.bfloat16).float().numpy()
-        dcs = Hx.cosine(got[b:b + 1] - xin[b:b + 1], want_q - xin[b:b + 1])
-        print(f"{kind}{' e4m3' if fp8 else ''} {wl.name} row {b}: max_abs {err:.4g} cos {cs:.7f} update-cos {dcs:.6f}")
-        if fp8:
-            assert err <= FP8_BLOCK_ATOL and cs >= BLOCK_COS and dcs >= FP8_UPDATE_COS, (b, err, cs, dcs)
-        else:
-            assert err <= BLOCK_ATOL and cs >= BLOCK_COS, (b, err, cs)
-            assert dcs >= 0.98, (b, dcs)
+            # parity: against the oracle's e4m3 path; accuracy: against the unquantised oracle
+            _check(f"{tag} e4m3-{e4m3} vs e4m3 oracle", got[b:b + 1], oracle(b, e4m3), xin[b:b + 1], Hx.E4M3_BARS,
+                   Hx.E4M3_ROWCOL_BARS if big else None)
+            _check(f"{tag} e4m3-{e4m3} vs unquantised oracle", got[b:b + 1], oracle(b, None), xin[b:b + 1],
+                   Hx.E4M3_ACCURACY_BARS)
 
 
 @pytest.mark.parametrize("kind", ["dual", "single"])
@@ -133,14 +138,15 @@ def _step(dit, wl, logical, inp, W=None):
     return vel, W
 
 
-def _oracle_step(wl, logical, inp, dt, rows):
+def _oracle_step(wl, logical, inp, dt, rows, e4m3=None):
     ow = Hx.oracle_weights(wl.widths, logical, dt)
     ids = O.token_ids(wl.n_txt, *wl.grid, wl.ref_grids)
     out = []
     for b in rows:
         ref = Hx.to_np(inp["ref_tokens"][b:b + 1], dt) if inp["ref_tokens"] is not None else None
         out.append(O.dit_step(ow, Hx.to_np(inp["img_tokens"][b:b + 1], dt), ref,
-                              Hx.to_np(inp["txt_emb"][b:b + 1], dt), Hx.to_np(inp["sigma"][b:b + 1]), ids, dt))
+                              Hx.to_np(inp["txt_emb"][b:b + 1], dt), Hx.to_np(inp["sigma"][b:b + 1]), ids, dt,
+                              e4m3=e4m3))
     return np.concatenate(out, 0)
 
 
@@ -171,8 +177,17 @@ def test_step_host_buffers_match_device_buffers(dit):
 
 
 def test_step_klein_1024(dit):
-    """The full 25-block step at 1024x1024 against the fp32 oracle (about a minute of CPU),
-    in bf16 and with every block projection in e4m3."""
+    """The full 25-block step at 1024x1024 against the fp32 oracle (a few minutes of CPU),
+    in bf16 and with every block projection in e4m3.
+
+    e4m3: over 25 blocks the quantiser decisions of the GPU and of the oracle's e4m3 path
+    stop coinciding (each block's small differences move inputs across rounding midpoints
+    in the next), so the two e4m3 velocities behave as two e4m3 roundings of one
+    computation.  The oracle alone gives the size of one: its e4m3 velocity sits at cosine
+    c0 from its unquantised velocity (computed here, ~0.990).  Two such roundings, each
+    1 - c0 away from the unquantised result, are about 2 (1 - c0) apart at most: the bar for
+    the GPU's e4m3 velocity against both the e4m3 and the unquantised oracle is
+    1 - 2 (1 - c0).  The element-wise e4m3 parity is in the block tests."""
     wl = synth.WORKLOADS["step_1024"]
     logical = synth.model_weights(wl.widths, seed=0)
     inp = synth.step_inputs(wl, seed=0)
@@ -181,12 +196,16 @@ def test_step_klein_1024(dit):
     vel8, W8 = _step(dit, wl, logical, inp, dit.DeviceWeights(wl.widths, logical, fp8=True))
     del W8
     want = _oracle_step(wl, logical, inp, np.float32, [0])
+    want8 = _oracle_step(wl, logical, inp, np.float32, [0], e4m3="all")
+    c0 = Hx.cosine(want8, want)
+    bar8 = 1.0 - 2.0 * (1.0 - c0)
     got, got8 = Hx.to_np(vel), Hx.to_np(vel8)
-    cs, cs8 = Hx.cosine(got, want), Hx.cosine(got8, want)
-    print(f"step_1024: cos {cs:.6f} max_abs {Hx.max_abs(got, want):.4g}; e4m3 projections: cos {cs8:.6f} "
-          f"max_abs {Hx.max_abs(got8, want):.4g}")
+    cs, cs8, cs8a = Hx.cosine(got, want), Hx.cosine(got8, want8), Hx.cosine(got8, want)
+    print(f"step_1024: cos {cs:.6f} max_abs {Hx.max_abs(got, want):.4g}; e4m3 oracle vs unquantised oracle: "
+          f"c0 {c0:.6f} (e4m3 bar {bar8:.5f}); GPU e4m3 vs e4m3 oracle: cos {cs8:.6f} max_abs "
+          f"{Hx.max_abs(got8, want8):.4g}; vs unquantised oracle: cos {cs8a:.6f}")
     assert cs >= STEP_COS
-    assert cs8 >= FP8_STEP_COS
+    assert cs8 >= bar8 and cs8a >= bar8
 
 
 def test_step_ref_b4_against_oracle_and_batch_invariance(dit):
@@ -323,6 +342,12 @@ REF3 = synth.Workload("ref3_1920x1088", synth.KLEIN, 1, 512, (68, 120), ((64, 64
 
 def test_dual_block_three_references_1920x1088(dit):
     run_block(dit, "dual", REF3, seed=3)
+
+
+def test_single_block_three_references_1920x1088(dit):
+    """The single-stream block (20 of the 25 blocks: fused QKV + MLP-in epilogue, attention
+    over 163 key blocks) at klein width with the three references, N = 20 832."""
+    run_block(dit, "single", REF3, seed=3)
 
 
 # A wider configuration through the same config-driven path (hidden 4096, 32 heads, MLP
