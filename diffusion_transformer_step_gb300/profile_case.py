@@ -1,8 +1,11 @@
 """Small fixed cases for profiler captures: one dual-stream or single-stream block at the
-1024x1024 shape (512 text + 4096 image tokens, hidden 3072), run `--reps` times through
-the C ABI.  About 1 GB on the device; the block GEMMs read more than the 129 MB L2.
+1024x1024 shape (512 text + 4096 image tokens, hidden 3072), or the per-step modulation at
+klein width (batch 1), run `--reps` times through the C ABI.  About 1 GB on the device for
+a block (its GEMMs read more than the 129 MB L2); 341 MB of modulation weights for the
+modulation.
 
     python -m diffusion_transformer_step_gb300.profile_case --block single --reps 2
+    python -m diffusion_transformer_step_gb300.profile_case --block modulation --reps 3
 """
 import argparse
 
@@ -13,7 +16,7 @@ from diffusion_transformer_step_gb300 import build_lib, dit, synth
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--block", choices=["single", "dual"], default="single")
+    ap.add_argument("--block", choices=["single", "dual", "modulation"], default="single")
     ap.add_argument("--reps", type=int, default=2)
     args = ap.parse_args()
     build_lib.build()
@@ -21,6 +24,17 @@ def main():
     wl = synth.WORKLOADS["single_block_1024"]
     wd = wl.widths
     g = synth.generator(0, dev)
+    if args.block == "modulation":
+        W = dit.DeviceWeights(wd, {"mod": synth.mod_weights(wd, g, dev), "dual": [], "single": []}, device=dev)
+        sigma = torch.full((1,), 0.75, dtype=torch.float32, device=dev)
+        mod = torch.empty((1, 17 * wd.hidden), dtype=torch.bfloat16, device=dev)
+        ws = torch.zeros(1 << 20, dtype=torch.uint8, device=dev)
+        for _ in range(args.reps):
+            dit.dit_modulation(W.w, sigma, 1, mod, ws, ws.numel())
+        st, where = dit.dit_sync_status(ws)
+        assert st == dit.DIT_OK, f"device wait gave up at site {where:#x}"
+        print(f"profile_case modulation x{args.reps}: ok")
+        return
     if args.block == "dual":
         logical = {"dual": [(synth.stream_weights(wd, g, dev), synth.stream_weights(wd, g, dev))], "single": []}
     else:
