@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) adaln_kernel(AdaLNArgs a) {
   long long consumed = 0;
   for (int i = 0; r < total; ++i, r += stride) {
     const int st = i & 1;
-    bool ok = mbar_wait(&bar[st], (uint32_t)(i >> 1) & 1u, wc, kSiteAdaLN);
+    bool ok = mbar_wait_sleep(&bar[st], (uint32_t)(i >> 1) & 1u, wc, kSiteAdaLN);
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) break;
     const uint8_t* buf = st ? buf1 : buf0;

@@ -43,7 +43,7 @@ const char* kernel_class_name(int cls) {
   return (cls >= 0 && cls < kClsCount) ? names[cls] : "?";
 }
 
-LaunchScope::LaunchScope(int cls, cudaStream_t stream) : slot_(-1), stream_(stream) {
+LaunchScope::LaunchScope(int cls, cudaStream_t stream) : slot_(-1), stream_(stream), captured_(t_capturing) {
   if (t_capturing)
     ++t_captured;
   else
@@ -52,12 +52,21 @@ LaunchScope::LaunchScope(int cls, cudaStream_t stream) : slot_(-1), stream_(stre
   if (g_timing_on && ((g_timing_mask >> cls) & 1u) && g_rec_used < (int)g_recs.size()) {
     slot_ = g_rec_used++;
     g_recs[slot_].cls = cls;
-    cudaEventRecord(g_recs[slot_].start, stream);
+    record(g_recs[slot_].start);
   }
 }
 
 LaunchScope::~LaunchScope() {
-  if (slot_ >= 0) cudaEventRecord(g_recs[slot_].stop, stream_);
+  if (slot_ >= 0) record(g_recs[slot_].stop);
+}
+
+// While a step is being captured, the event pair becomes a pair of event-record nodes of
+// the graph (re-recorded on every replay), so a replayed step can be timed per launch too.
+void LaunchScope::record(cudaEvent_t e) {
+  if (captured_)
+    cudaEventRecordWithFlags(e, stream_, cudaEventRecordExternal);
+  else
+    cudaEventRecord(e, stream_);
 }
 
 bool pdl_enabled() {

@@ -31,16 +31,19 @@ enum KernelClass : int {
 
 const char* kernel_class_name(int cls);
 
-// Brackets one kernel launch: counts it and, while timing is on, records an event
-// pair on the launch's stream.
+// Brackets one kernel launch: counts it (or, during a graph capture on this thread, adds it
+// to the graph's count) and, while timing is on, records an event pair on the launch's
+// stream (captured into the graph during a capture).
 class LaunchScope {
  public:
   LaunchScope(int cls, cudaStream_t stream);
   ~LaunchScope();
 
  private:
+  void record(cudaEvent_t e);
   int slot_;
   cudaStream_t stream_;
+  bool captured_;
 };
 
 // Number of SMs of the current device (cached per device).

@@ -366,7 +366,10 @@ unsigned long long dit_launch_count(void);
 
 /* Start recording a CUDA event pair around every kernel launch (up to max_records
  * launches), tagged with the kernel's class (dit_kernel_class_name).  Events are
- * recorded on the launch's own stream. */
+ * recorded on the launch's own stream.  A step captured by dit_step_graph_create while
+ * recording is on carries its event pairs as event-record nodes: each replay records them
+ * again (the records then hold the latest replay's times), so destroy such a graph before
+ * the next dit_timing_begin, which releases the events. */
 dit_status dit_timing_begin(int max_records);
 
 /* Restrict the event pairs of dit_timing_begin to launches whose class bit is set in
