@@ -1,7 +1,7 @@
 // Persistent tcgen05 GEMM with fused epilogues: out = A W^T, A [rows, k] and W [n, k]
 // both K-major bf16, fp32 accumulation in Tensor Memory.
 //
-// CTA pairs (clusters of 2, tcgen05 cta_group::2), one CTA per SM, 192 threads each.  A
+// CTA pairs (clusters of 2, tcgen05 cta_group::2), one CTA per SM, 320 threads each.  A
 // pair computes a 256 x 256 tile: CTA r loads rows [128r, 128r + 128) of the A tile and
 // rows [128r, 128r + 128) of the W tile, so each CTA streams 32 KB per 64-deep k-block
 // (a 1-CTA 128 x 256 tile needs 48 KB for half the work) and 6 stages fit in shared memory.
@@ -13,9 +13,15 @@
 //               per CTA) and, in the leader only, issues tcgen05.mma.cta_group::2 (M=256,
 //               N=256, K=16) from one thread; commits are multicast to both CTAs' empty
 //               and accumulator-full barriers;
-//   warps 2-5   epilogue in both CTAs: one thread per accumulator row of its own CTA,
-//               tcgen05.ld 32 columns at a time, fused math, 16-byte global stores; the
-//               accumulator is handed back on the leader's barrier (8 arrivals).
+//   warps 2-9   epilogue in both CTAs: two warps per TMEM lane quarter, each taking one
+//               128-column half of the accumulator (one QKV head, one half of the SwiGLU
+//               outputs, four 32-column chunks of a residual or plain store), one thread per
+//               accumulator row of its own CTA, tcgen05.ld 32 columns at a time, fused math,
+//               16-byte global stores; the accumulator is handed back on the leader's
+//               barrier (16 arrivals).  Two warps per row keep a tile's epilogue shorter
+//               than the next tile's main loop even for K = 3072 with an fp32 residual
+//               output, where one warp per row (its loads of the residual serialised chunk
+//               by chunk) took 18 us against a 14.5 us main loop and held the MMAs back.
 // The two accumulators let tile i's epilogue overlap tile i+1's main loop.  Because the
 // MMA-issuing warp competes for issue slots with the epilogue warp of its SM sub-partition
 // (on sm_103a dense scalar FP32 FMA there slows tcgen05.mma issue several-fold, packed
@@ -46,7 +52,7 @@ namespace {
 constexpr int BM = 128, BN = 256, BK = 64;   // per CTA: 128 rows of A; the pair's tile is 256 x 256
 constexpr int PAIR_M = 2 * BM;
 constexpr int kStages = 6;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr uint32_t kATileBytes = BM * BK * 2;        // 16 KB (this CTA's half of A)
 constexpr uint32_t kBTileBytes = (BN / 2) * BK * 2;  // 16 KB (this CTA's half of B)
 constexpr uint32_t kStageBytes = kATileBytes + kBTileBytes;
@@ -238,11 +244,12 @@ __device__ __forceinline__ void load_row32_f32(const float* src, float* f) {
 
 // SwiGLU over one packed 256-column accumulator: 128 outputs at dst[0..128).
 // silu(g) = g / (1 + 2^(-g log2 e)) with MUFU ex2 and rcp.approx.
+// Chunks [c_begin, c_end) of the 4 (one epilogue warp takes two).
 __device__ __forceinline__ void epi_swiglu(uint32_t tbase, bool row_ok, bf16* dst, int cols_left, const Dequant& dq,
-                                           int col0) {
+                                           int col0, int c_begin, int c_end) {
   const float2 nl2e = f2(-1.4426950408889634f, -1.4426950408889634f), one = f2(1.0f, 1.0f);
 #pragma unroll 1
-  for (int c = 0; c < 4; ++c) {
+  for (int c = c_begin; c < c_end; ++c) {
     uint32_t g[32], u[32];
     tmem_load32(tbase + c * 32, g);
     tmem_load32(tbase + 128 + c * 32, u);
@@ -354,7 +361,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], 8);  // 4 epilogue warps in each CTA of the pair
+      mbar_init(&acc_empty[a], 16);  // 8 epilogue warps in each CTA of the pair
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -477,6 +484,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;
+    const int eh = (warp - 2) >> 2;  // the 128-column half of the accumulator this warp takes
     const uint32_t acc_empty_leader0 = map_to_rank(smem_u32(&acc_empty[0]), 0);
     const uint32_t acc_empty_leader1 = map_to_rank(smem_u32(&acc_empty[1]), 0);
     int local = 0;
@@ -503,7 +511,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const bf16* grow = pr.gate ? pr.gate + (long long)ti.b * pr.gate_stride + col0 : nullptr;
         const float gsc = pr.coef ? pr.coef[ti.b] : 0.f;
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = eh * 4; c < eh * 4 + 4; ++c) {
           uint32_t v[32];
           tmem_load32(tbase + c * 32, v);
           if (kFp8 && col0 + c * 32 < pr.n) dequant32(v, dq, col0 + c * 32);
@@ -544,7 +552,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int n_out = (pr.n - (pr.epi == kEpiQKV ? pr.n_qkv : 0)) / 2;
         bf16* orow = pr.out + (long long)ti.b * pr.out_bstride + (long long)(pr.out_row0 + r) * pr.ld_out +
                      pr.out_col0 + ocol;
-        epi_swiglu(tbase, row_ok, orow, n_out - ocol, dq, col0);
+        epi_swiglu(tbase, row_ok, orow, n_out - ocol, dq, col0, 2 * eh, 2 * eh + 2);
       } else {
         const int which = col0 / pr.hidden;
         const int heads = pr.hidden / 128;
@@ -553,7 +561,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const bf16* nw = which == 0 ? pr.q_norm : pr.k_norm;
         const float* rope_row = pr.rope + (long long)(row_ok ? tok : 0) * 128;
 #pragma unroll 1
-        for (int hh = 0; hh < BN / 128; ++hh) {
+        for (int hh = eh; hh < eh + 1; ++hh) {
           const int head = (col0 % pr.hidden) / 128 + hh;
           bf16* dst = base + (((long long)ti.b * heads + head) * pr.seq + tok) * 128;
           epi_qkv_head(tbase + hh * 128, row_ok, which, dst, nw, rope_row, P.eps, dq, col0 + hh * 128);
