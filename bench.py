@@ -64,9 +64,9 @@ BF16_FLOP_PER_CLK_PER_SM = 8192.0
 # DRAM traffic per launch of the dominant kernel from one ncu capture (see profiles/);
 # None until captured for the current kernel.
 NCU_TRAFFIC = {
-    # profiles/gemm_fused_qkv_mlp__single_block_1024.md: dram read 205.24 MB + write 154.12 MB
-    # for one launch of the same shape as in the step (M 4608, N 27648, K 3072)
-    "gemm_fused_qkv_mlp": 359358464,
+    # profiles/gemm_fused_qkv_mlp__single_block_1024.md: dram read 205.67 MB + write 153.83 MB
+    # for one launch of the same shape as in the step (M 4608, N 27648, K 3072), current kernel
+    "gemm_fused_qkv_mlp": 359505920,
 }
 
 
@@ -269,6 +269,46 @@ def whole_job_steps_per_s(ms_per_step_max: float, world: int) -> float:
     return world / (ms_per_step_max / 1e3)
 
 
+def hbm_kernels_alone(torch, dit, W, wl, stream, ws, nbytes, reps=20):
+    """Mean time of dit_modulation (the step's batch) and of one bf16 dit_adaln pass over
+    the step's B x N rows, each timed alone with CUDA events around `reps` back-to-back
+    calls after a warm-up; bytes as in step_class_bytes (weights once; rows read and
+    written once)."""
+    wd = wl.widths
+    H, N, B = wd.hidden, wl.n_tokens, wl.batch
+    dev = ws.device
+    sigma = torch.full((B,), 0.75, dtype=torch.float32, device=dev)
+    mod = torch.empty((B, 17 * H), dtype=torch.bfloat16, device=dev)
+    x = torch.randn((B, N, H), device=dev).to(torch.bfloat16)
+    y = torch.empty_like(x)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    ms_mod = timed(lambda: dit.dit_modulation(W.w, sigma, B, mod, ws, nbytes, stream))
+    ms_ln = timed(lambda: dit.dit_adaln(B, N, H, x, N, 0, N, mod[:, :H], mod[:, H:2 * H], mod[:, :H], mod[:, H:2 * H],
+                                        17 * H, 1e-6, y, stream))
+    st, where = dit.dit_sync_status(ws, stream)
+    if st != dit.DIT_OK:
+        raise RuntimeError(f"device wait gave up at site {where:#x}")
+    b_mod = (H * wd.time_dim + H * H + 17 * H * H) * 2
+    b_ln = 2 * B * N * H * 2
+    return {"what": f"each timed alone, {reps} back-to-back calls with CUDA events around them",
+            "modulation": {"us_per_call": round(ms_mod * 1e3, 2), "bytes": b_mod,
+                           "gbs": round(b_mod / (ms_mod / 1e3) / 1e9, 1)},
+            "adaln_bf16": {"us_per_call": round(ms_ln * 1e3, 2), "bytes": b_ln,
+                           "gbs": round(b_ln / (ms_ln / 1e3) / 1e9, 1)}}
+
+
 # ---------------------------------------------------------------------------------- CPU oracle
 def oracle_blocks(wl, seed=0):
     """Set up one dual-stream and one single-stream block of the fp32 oracle at wl's shape
@@ -451,6 +491,13 @@ def run_ours(args, wl, rank, world, local_rank):
     ms_step = reduce_max(ms_total, world, dev) / args.steps
     value = whole_job_steps_per_s(ms_step, world)
 
+    # ---- the HBM-bound kernels timed alone through their entry points (the in-step
+    #      breakdown above has an event pair around every one of their short launches):
+    #      the whole modulation as one call, and one adaLN pass over the step's rows
+    hbm_alone = None
+    if rank == 0:
+        hbm_alone = hbm_kernels_alone(torch, dit, W, wl, stream, ws, nbytes)
+
     # ---- host cost of enqueueing one step (direct call, GPU idle before and after)
     host_ms = []
     for _ in range(3):
@@ -552,6 +599,9 @@ def run_ours(args, wl, rank, world, local_rank):
                "dual_block_s": round(smp["dual_block_s"], 3), "single_block_s": round(smp["single_block_s"], 3),
                "step_s_scaled": round(smp["step_s_scaled"], 2)}
 
+    if hbm_alone is not None and peak_get(peaks, "hbm_gbs"):
+        for k in ("modulation", "adaln_bf16"):
+            hbm_alone[k]["frac_of_hbm"] = round(hbm_alone[k]["gbs"] / peak_get(peaks, "hbm_gbs"), 4)
     line = {"metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded random weights and inputs)",
@@ -576,7 +626,7 @@ def run_ours(args, wl, rank, world, local_rank):
                         "projection bf16; not the headline",
                 "value": round(whole_job_steps_per_s(fp8_ms_step, world), 4), "unit": UNIT,
                 "ms_per_step": round(fp8_ms_step, 4)},
-            "gpu_launches": launches, "clocks": clocks}
+            "hbm_kernels_alone": hbm_alone, "gpu_launches": launches, "clocks": clocks}
     print(json.dumps(line), flush=True)
 
 
