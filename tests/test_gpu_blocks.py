@@ -416,3 +416,32 @@ def test_concurrent_steps_from_two_host_threads(dit):
         st, where = dit.dit_sync_status(ws, s)
         assert st == dit.DIT_OK, f"device wait gave up at site {where:#x}"
         assert torch.equal(vel, want[i]), i
+
+
+@pytest.mark.parametrize("fp8", [False, "all"], ids=["bf16", "e4m3"])
+def test_step_ignores_stale_workspace_and_writes_only_its_output(dit, fp8):
+    """Every scratch value a step reads it has written first: a workspace filled with 0xFF
+    bytes (NaN in every bf16 / fp32 view, 0xFF in every e4m3 code) outside its zeroed status
+    word gives the same velocity, bit for bit, as a zeroed workspace.  A guard region past
+    the velocity buffer keeps its canary values."""
+    wl = TINY_REF
+    logical = synth.model_weights(wl.widths, seed=13)
+    inp = synth.step_inputs(wl, seed=13)
+    W = dit.DeviceWeights(wl.widths, logical, fp8=fp8)
+    shape, rope, ws, nbytes = _setup(dit, wl, W)
+    n_vel = wl.batch * wl.n_img * wl.widths.in_channels
+    guard = 4096
+    outs = []
+    for fill in (0x00, 0xFF):
+        ws.fill_(fill)
+        ws[:256].zero_()  # the status word: zeroed once by the caller
+        buf = torch.full((n_vel + guard,), 12345.0, dtype=torch.bfloat16, device=DEV)
+        vel = buf[:n_vel].view(wl.batch, wl.n_img, wl.widths.in_channels)
+        ref = inp["ref_tokens"].to(DEV) if inp["ref_tokens"] is not None else None
+        dit.dit_step_fwd(W.w, shape, inp["img_tokens"].to(DEV), ref, inp["txt_emb"].to(DEV), rope,
+                         inp["sigma"].to(DEV), vel, ws, nbytes)
+        _status(dit, ws)
+        assert torch.isfinite(vel.float()).all()
+        assert (buf[n_vel:] == 12345.0).all()
+        outs.append(vel.clone())
+    assert torch.equal(outs[0], outs[1])
