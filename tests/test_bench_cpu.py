@@ -62,3 +62,30 @@ def test_kernel_breakdown_rates_and_shares():
     assert k["gemm_fused_qkv_mlp"]["tflops"] == pytest.approx(7.83e11 / 0.43e-3 / 1e12, abs=0.1)
     assert sum(v["share"] for v in k.values()) == pytest.approx(1.0, abs=1e-3)
     assert bench.kernel_breakdown(recs, flops, {"adaln": 1e9}, 2, None)["adaln"]["frac_of_hbm"] is None
+
+
+def test_dense_peak_at_clock_and_the_oracle_sample_scaling():
+    """The clock-scaled dense peak is SMs x 8192 FLOP per clock x the clock (152 SMs at
+    1691 MHz: 2105.6 TFLOP/s), and no clock sample gives none; the CPU sample's scaling to a
+    whole step is 5 dual + 20 single block times."""
+    class Props:
+        multi_processor_count = 152
+    p = bench.dense_peak_at_clock(1691.0, Props())
+    assert p["tflops"] == pytest.approx(152 * 8192 * 1691e6 / 1e12, abs=0.05) and p["sms"] == 152
+    assert bench.dense_peak_at_clock(None, Props()) is None
+    wl = synth.WORKLOADS["tiny"]
+    calls = []
+
+    def fake_blocks(w, seed=0):
+        assert w is wl
+        return lambda: calls.append(1) or (2.0, 3.0)
+
+    orig = bench.oracle_blocks
+    bench.oracle_blocks = fake_blocks
+    try:
+        smp = bench.oracle_sample(wl, reps=2)
+    finally:
+        bench.oracle_blocks = orig
+    nd, ns = wl.widths.n_dual, wl.widths.n_single
+    assert len(calls) == 2 and smp["dual_block_s"] == 2.0 and smp["single_block_s"] == 3.0
+    assert smp["step_s_scaled"] == nd * 2.0 + ns * 3.0 and smp["sample_s"] == 5.0
