@@ -86,16 +86,22 @@ def test_adaln(dit, hidden, rows, split, batch):
     _cmp(y, want)
 
 
-@pytest.mark.parametrize("wd", [synth.TINY, synth.KLEIN])
-@pytest.mark.parametrize("batch", [1, 3])
+WIDE_MOD = synth.Widths(hidden=4096, heads=32, head_dim=128, mlp_hidden=12288, n_dual=1, n_single=1)
+
+
+@pytest.mark.parametrize("wd,batch", [(synth.TINY, 1), (synth.TINY, 3), (synth.KLEIN, 1), (synth.KLEIN, 3),
+                                      (synth.KLEIN, 11), (WIDE_MOD, 8)],
+                         ids=lambda v: getattr(v, "hidden", v))
 def test_modulation(dit, wd, batch, ws):
+    """Every element of the modulation vector against the oracle; batch 11 runs as launches
+    of 8 and 3 rows, batch 8 at hidden 4096 fills one launch's largest instantiation."""
     g = synth.generator(7)
     mw = synth.mod_weights(wd, g)
     w = dit.dit_weights()
     w.cfg = dit.make_config(hidden=wd.hidden, heads=wd.heads, mlp_hidden=wd.mlp_hidden)
     dev = {k: v.to(DEV) for k, v in mw.items()}
     w.mod.t_in, w.mod.t_out, w.mod.mod = dev["t_in"].data_ptr(), dev["t_out"].data_ptr(), dev["mod"].data_ptr()
-    sigma = torch.tensor([0.93, 0.51, 0.0][:batch], dtype=torch.float32)
+    sigma = torch.tensor([0.93, 0.51, 0.0, 1.0, 0.25, 0.7, 0.33, 0.05, 0.88, 0.6, 0.12][:batch], dtype=torch.float32)
     out = torch.empty((batch, 17 * wd.hidden), dtype=torch.bfloat16, device=DEV)
     dit.dit_modulation(w, sigma.to(DEV), batch, out, ws, ws.numel())
     _check_status(dit, ws)
