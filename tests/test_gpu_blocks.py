@@ -181,6 +181,29 @@ def test_step_tiny_e4m3(dit, wl):
     assert cs8 >= bar8
 
 
+def test_step_at_the_largest_batch(dit):
+    """Batch 64, the largest the library accepts, each row with its own sigma (the
+    modulation runs as eight launches of eight rows; the attention grid's z extent is 64):
+    rows 0 and 63 against the oracle, and rows 0, 31 and 63 equal, bit for bit, to the
+    batch-1 step of the same row (rows are independent)."""
+    wl = synth.Workload("tiny_b64", synth.TINY, 64, 8, (2, 3), ((1, 2),))
+    logical = synth.model_weights(wl.widths, seed=14)
+    inp = synth.step_inputs(wl, seed=14)
+    inp["sigma"] = torch.linspace(0.02, 1.0, 64, dtype=torch.float32)
+    vel, W = _step(dit, wl, logical, inp)
+    got = Hx.to_np(vel)
+    want = _oracle_step(wl, logical, inp, np.float64, [0, 63])
+    for i, b in enumerate((0, 63)):
+        cs = Hx.cosine(got[b], want[i])
+        print(f"batch 64 row {b}: cos {cs:.6f}")
+        assert cs >= STEP_COS, (b, cs)
+    one_wl = synth.Workload("row", wl.widths, 1, wl.n_txt, wl.grid, wl.ref_grids)
+    for b in (0, 31, 63):
+        one = {k: (v[b:b + 1].clone() if v is not None else None) for k, v in inp.items()}
+        v1, _ = _step(dit, one_wl, logical, one, W)
+        assert torch.equal(v1[0], vel[b]), b
+
+
 def test_step_host_buffers_match_device_buffers(dit):
     wl = TINY_REF
     logical = synth.model_weights(wl.widths, seed=4)
