@@ -6,6 +6,10 @@ modulation.
 
     python -m diffusion_transformer_step_gb300.profile_case --block single --reps 2
     python -m diffusion_transformer_step_gb300.profile_case --block modulation --reps 3
+    python -m diffusion_transformer_step_gb300.profile_case --block single --fp8 --reps 2
+
+`--fp8` runs the block with every projection in e4m3 (per-row activation and per-output-channel
+weight scales, the library's low-precision variant).
 """
 import argparse
 
@@ -18,6 +22,7 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--block", choices=["single", "dual", "modulation"], default="single")
     ap.add_argument("--reps", type=int, default=2)
+    ap.add_argument("--fp8", action="store_true", help="every block projection in e4m3")
     args = ap.parse_args()
     build_lib.build()
     dev = "cuda"
@@ -39,7 +44,7 @@ def main():
         logical = {"dual": [(synth.stream_weights(wd, g, dev), synth.stream_weights(wd, g, dev))], "single": []}
     else:
         logical = {"dual": [], "single": [synth.single_weights(wd, g, dev)]}
-    W = dit.DeviceWeights(wd, logical, device=dev)
+    W = dit.DeviceWeights(wd, logical, device=dev, fp8="all" if args.fp8 else False)
     bi = synth.block_inputs(wl, 0, dev)
     shape = dit.make_shape(wl.batch, wl.n_txt, wl.n_img, wl.n_ref)
     ids = dit.dit_token_ids(shape, *wl.grid)
@@ -53,7 +58,7 @@ def main():
         fwd(W.w, 0, shape, bi["x"], bi["mod"], rope, ws, nbytes)
     st, where = dit.dit_sync_status(ws)
     assert st == dit.DIT_OK, f"device wait gave up at site {where:#x}"
-    print(f"profile_case {args.block} x{args.reps}: ok")
+    print(f"profile_case {args.block}{' e4m3' if args.fp8 else ''} x{args.reps}: ok")
 
 
 if __name__ == "__main__":
