@@ -527,12 +527,13 @@ def euler_update(x, v, sigma_cur, sigma_next):
     return x + (sigma_next - sigma_cur) * v
 
 
-def denoise(w: Weights, x0, ref_tokens, txt_emb, ids, sigmas, dtype=np.float64):
-    """The 4-step loop ([card]: steps fixed at 4, each step one DiT call)."""
+def denoise(w: Weights, x0, ref_tokens, txt_emb, ids, sigmas, dtype=np.float64, e4m3=None):
+    """The 4-step loop ([card]: steps fixed at 4, each step one DiT call).  e4m3 is passed to
+    every step (reading R26 of the precision knob); the Euler update itself is unquantised."""
     x = np.asarray(x0).astype(dtype)
     B = x.shape[0]
     for k in range(len(sigmas) - 1):
-        v = dit_step(w, x, ref_tokens, txt_emb, np.full(B, sigmas[k]), ids, dtype)
+        v = dit_step(w, x, ref_tokens, txt_emb, np.full(B, sigmas[k]), ids, dtype, e4m3=e4m3)
         x = euler_update(x, v, sigmas[k], sigmas[k + 1])
     return x
 

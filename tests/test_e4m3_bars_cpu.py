@@ -76,3 +76,25 @@ def test_e4m3_bars_reject_a_wrong_scale(monkeypatch, kind):
         print(kind, plant, idx, {k: round(v, 5) for k, v in mm.items()}, bad)
         assert bad, (kind, plant, idx, mm)
         assert ("col_err" in bad) if plant == "col" else ("row_err" in bad)
+
+
+def test_denoise_loop_passes_e4m3_to_every_step():
+    """The oracle's loop with the e4m3 option is the loop of e4m3 steps (the option reaches
+    every DiT call; the Euler update stays unquantised), and it differs from the unquantised
+    loop: the GPU e4m3 loop test compares against this."""
+    wl = synth.WORKLOADS["tiny"]
+    logical = synth.model_weights(wl.widths, seed=3)
+    inp = synth.step_inputs(wl, seed=3)
+    ow = Hx.oracle_weights(wl.widths, logical)
+    ids = O.token_ids(wl.n_txt, *wl.grid, wl.ref_grids)
+    sig = O.sigma_schedule(float(inp["sigma"][0]))
+    x0 = Hx.to_np(inp["img_tokens"])
+    txt = Hx.to_np(inp["txt_emb"])
+    got = O.denoise(ow, x0, None, txt, ids, sig, e4m3="all")
+    x = x0.astype(np.float64)
+    for k in range(len(sig) - 1):
+        v = O.dit_step(ow, x, None, txt, np.full(wl.batch, sig[k]), ids, e4m3="all")
+        x = O.euler_update(x, v, sig[k], sig[k + 1])
+    np.testing.assert_array_equal(got, x)
+    plain = O.denoise(ow, x0, None, txt, ids, sig)
+    assert np.abs(got - plain).max() > 0

@@ -351,6 +351,42 @@ def test_denoise_loop_tiny(dit, wl):
     assert cs >= 0.999 and dcs >= STEP_COS
 
 
+@pytest.mark.parametrize("wl", [synth.WORKLOADS["tiny"], TINY_REF], ids=lambda w: w.name)
+def test_denoise_loop_tiny_e4m3(dit, wl):
+    """The 4-step loop with every block projection in e4m3 against the oracle's e4m3 loop
+    (fp64): the displacement cosine at the e4m3 step bar, STEP_COS - 2 (1 - c0), c0 the
+    displacement cosine between the oracle's e4m3 and unquantised loops.  At these widths
+    e4m3 moves the result very little (c0 ~ 1 - 1e-9), so the test also checks that the
+    device loop took the e4m3 path: its result differs from the bf16 loop's."""
+    logical = synth.model_weights(wl.widths, seed=8)
+    inp = synth.step_inputs(wl, seed=8)
+    sig = _schedule(inp)
+    ref = inp["ref_tokens"].to(DEV) if inp["ref_tokens"] is not None else None
+    outs = {}
+    for fp8 in (False, True):
+        W = dit.DeviceWeights(wl.widths, logical, fp8=fp8)
+        shape, rope, ws, nbytes = _setup(dit, wl, W)
+        xd = inp["img_tokens"].to(DEV).clone()
+        dit.dit_denoise_fwd(W.w, shape, xd, ref, inp["txt_emb"].to(DEV), rope, sig.tolist(), ws, nbytes)
+        _status(dit, ws)
+        outs[fp8] = xd
+    x = outs[True]
+    assert not torch.equal(outs[True], outs[False])
+    ow = Hx.oracle_weights(wl.widths, logical)
+    ids = O.token_ids(wl.n_txt, *wl.grid, wl.ref_grids)
+    x0 = Hx.to_np(inp["img_tokens"])
+    args = (Hx.to_np(inp["ref_tokens"]), Hx.to_np(inp["txt_emb"]), ids, sig.astype(np.float64))
+    want8 = O.denoise(ow, x0, *args, e4m3="all")
+    want = O.denoise(ow, x0, *args)
+    c0 = Hx.cosine(want8 - x0, want - x0)
+    bar8 = STEP_COS - 2.0 * (1.0 - c0)
+    got = Hx.to_np(x)
+    dcs8 = Hx.cosine(got - x0, want8 - x0)
+    print(f"denoise {wl.name} e4m3: displacement-cos vs e4m3 oracle {dcs8:.6f} (bar {bar8:.6f}, c0 {c0:.9f}), "
+          f"vs unquantised {Hx.cosine(got - x0, want - x0):.6f}")
+    assert dcs8 >= bar8
+
+
 def test_denoise_loop_matches_stepwise_klein_1024(dit):
     """At the full 1024x1024 shape the device loop equals four dit_step_fwd calls with the
     Euler update applied outside (fp32 latent, bf16 input to each step)."""
