@@ -77,6 +77,15 @@ def run_block(dit, kind, wl, seed=0, check_rows=None, fp8=False):
     fwd(W.w, 0, shape, x, mod, rope, ws, nbytes)
     _status(dit, ws)
     got = Hx.to_np(x)
+    if fp8:
+        # the e4m3 effect can sit inside the parity bars (at tiny widths the update moves by
+        # ~0.998 in cosine): check that the block took the e4m3 path, against the same block
+        # in bf16
+        W16 = dit.DeviceWeights(wd, logical)
+        x16 = bi["x"].to(DEV).contiguous()
+        fwd(W16.w, 0, shape, x16, mod, rope, ws, nbytes)
+        _status(dit, ws)
+        assert not torch.equal(x16, x)
 
     big = wd.hidden > 1024
     dt = np.float32 if big else np.float64
@@ -170,6 +179,10 @@ def test_step_tiny_e4m3(dit, wl):
     logical = synth.model_weights(wl.widths, seed=5)
     inp = synth.step_inputs(wl, seed=5)
     vel, _ = _step(dit, wl, logical, inp, dit.DeviceWeights(wl.widths, logical, fp8=True))
+    # at these widths e4m3 moves the velocity very little (c0 ~ 1 - 4e-9): check that the
+    # step took the e4m3 path at all, against the same step in bf16
+    vel_bf16, _ = _step(dit, wl, logical, inp, dit.DeviceWeights(wl.widths, logical))
+    assert not torch.equal(vel, vel_bf16)
     want8 = _oracle_step(wl, logical, inp, np.float64, range(wl.batch), e4m3="all")
     want = _oracle_step(wl, logical, inp, np.float64, range(wl.batch))
     c0 = Hx.cosine(want8, want)
