@@ -89,51 +89,53 @@ def normal(shape, std, gen, device="cpu", mean=0.0, draw_dtype=torch.float32) ->
     return (t * std + mean).to(torch.bfloat16)
 
 
-def mod_weights(wd: Widths, gen, device="cpu", draw_dtype=torch.float32) -> dict:
+def mod_weights(wd: Widths, gen, device="cpu", draw_dtype=torch.float32, mod_std=WEIGHT_STD) -> dict:
     H = wd.hidden
     return {
         "t_in": normal((H, wd.time_dim), WEIGHT_STD, gen, device, draw_dtype=draw_dtype),
         "t_out": normal((H, H), WEIGHT_STD, gen, device, draw_dtype=draw_dtype),
-        "mod": normal((17 * H, H), WEIGHT_STD, gen, device, draw_dtype=draw_dtype),
+        "mod": normal((17 * H, H), mod_std, gen, device, draw_dtype=draw_dtype),
     }
 
 
-def stream_weights(wd: Widths, gen, device="cpu", draw_dtype=torch.float32) -> dict:
+def stream_weights(wd: Widths, gen, device="cpu", draw_dtype=torch.float32, std=WEIGHT_STD) -> dict:
     H, F, D = wd.hidden, wd.mlp_hidden, wd.head_dim
     return {
-        "qkv": normal((3 * H, H), WEIGHT_STD, gen, device, draw_dtype=draw_dtype),
+        "qkv": normal((3 * H, H), std, gen, device, draw_dtype=draw_dtype),
         "q_norm": normal((D,), WEIGHT_STD, gen, device, mean=1.0, draw_dtype=draw_dtype),
         "k_norm": normal((D,), WEIGHT_STD, gen, device, mean=1.0, draw_dtype=draw_dtype),
-        "out": normal((H, H), WEIGHT_STD, gen, device, draw_dtype=draw_dtype),
-        "mlp_in": normal((2 * F, H), WEIGHT_STD, gen, device, draw_dtype=draw_dtype),
-        "mlp_out": normal((H, F), WEIGHT_STD, gen, device, draw_dtype=draw_dtype),
+        "out": normal((H, H), std, gen, device, draw_dtype=draw_dtype),
+        "mlp_in": normal((2 * F, H), std, gen, device, draw_dtype=draw_dtype),
+        "mlp_out": normal((H, F), std, gen, device, draw_dtype=draw_dtype),
     }
 
 
-def single_weights(wd: Widths, gen, device="cpu", draw_dtype=torch.float32) -> dict:
+def single_weights(wd: Widths, gen, device="cpu", draw_dtype=torch.float32, std=WEIGHT_STD) -> dict:
     H, F, D = wd.hidden, wd.mlp_hidden, wd.head_dim
     return {
-        "qkv_mlp": normal((3 * H + 2 * F, H), WEIGHT_STD, gen, device, draw_dtype=draw_dtype),
+        "qkv_mlp": normal((3 * H + 2 * F, H), std, gen, device, draw_dtype=draw_dtype),
         "q_norm": normal((D,), WEIGHT_STD, gen, device, mean=1.0, draw_dtype=draw_dtype),
         "k_norm": normal((D,), WEIGHT_STD, gen, device, mean=1.0, draw_dtype=draw_dtype),
-        "out": normal((H, H + F), WEIGHT_STD, gen, device, draw_dtype=draw_dtype),
+        "out": normal((H, H + F), std, gen, device, draw_dtype=draw_dtype),
     }
 
 
 def model_weights(wd: Widths, seed: int, device="cpu", n_dual=None, n_single=None,
-                  draw_dtype=torch.float32) -> dict:
-    """Every weight of the model, logical layouts, bf16."""
+                  draw_dtype=torch.float32, block_std=WEIGHT_STD, mod_std=WEIGHT_STD) -> dict:
+    """Every weight of the model, logical layouts, bf16.  block_std (the blocks' projection
+    matrices) and mod_std (the 17H modulation projection) scale the same draws; the defaults
+    are the recipe's 0.02."""
     g = generator(seed, device)
     H, C = wd.hidden, wd.in_channels
-    w = {"mod": mod_weights(wd, g, device, draw_dtype=draw_dtype),
+    w = {"mod": mod_weights(wd, g, device, draw_dtype=draw_dtype, mod_std=mod_std),
          "x_emb": normal((H, C), WEIGHT_STD, g, device, draw_dtype=draw_dtype),
          "ctx_emb": normal((H, wd.txt_dim), WEIGHT_STD, g, device, draw_dtype=draw_dtype),
          "proj_out": normal((C, H), WEIGHT_STD, g, device, draw_dtype=draw_dtype)}
     nd = wd.n_dual if n_dual is None else n_dual
     ns = wd.n_single if n_single is None else n_single
-    w["dual"] = [(stream_weights(wd, g, device, draw_dtype=draw_dtype),
-                  stream_weights(wd, g, device, draw_dtype=draw_dtype)) for _ in range(nd)]
-    w["single"] = [single_weights(wd, g, device, draw_dtype=draw_dtype) for _ in range(ns)]
+    w["dual"] = [(stream_weights(wd, g, device, draw_dtype=draw_dtype, std=block_std),
+                  stream_weights(wd, g, device, draw_dtype=draw_dtype, std=block_std)) for _ in range(nd)]
+    w["single"] = [single_weights(wd, g, device, draw_dtype=draw_dtype, std=block_std) for _ in range(ns)]
     return w
 
 
