@@ -216,7 +216,7 @@ def test_step_at_the_largest_batch(dit):
     rows 0 and 63 against the oracle, and rows 0, 31 and 63 equal, bit for bit, to the
     batch-1 step of the same row (rows are independent)."""
     wl = synth.Workload("tiny_b64", synth.TINY, 64, 8, (2, 3), ((1, 2),))
-    logical = synth.model_weights(wl.widths, seed=14)
+    logical = _tiny_step_weights(wl, seed=14)
     inp = synth.step_inputs(wl, seed=14)
     inp["sigma"] = torch.linspace(0.02, 1.0, 64, dtype=torch.float32)
     vel, W = _step(dit, wl, logical, inp)
