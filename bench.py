@@ -588,9 +588,9 @@ def run_ours(args, wl, rank, world, local_rank):
     flops = step_flops(wd, wl.batch, wl.n_txt, wl.n_img, wl.n_ref)
     tflops = flops / (ms_step / 1e3) / 1e12
 
-    # ---- CPU oracle baseline on a bounded sample
+    # ---- CPU oracle baseline on a bounded sample (rank 0 of a one-GPU run only)
     cpu = None
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and world == 1:
         smp = oracle_sample(wl)
         cpu = {"value": wl.batch / smp["step_s_scaled"], "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
                "sample": f"one dual-stream ({smp['dual_block_s']:.2f} s) and one single-stream "
