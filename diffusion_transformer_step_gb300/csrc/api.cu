@@ -892,7 +892,9 @@ dit_status dit_selftest_wait_timeout(void* ws, size_t ws_bytes, unsigned int lim
 dit_status dit_adaln(int batch, int rows, int hidden, const void* x_dev, int x_rows, int x_row0, int split,
                      const void* shift_lo, const void* scale_lo, const void* shift_hi, const void* scale_hi,
                      long long mod_stride, float eps, void* y_dev, dit_stream_t stream) {
-  if (batch < 1 || rows < 0 || x_rows < 0 || x_row0 < 0 || (long long)x_row0 + rows > x_rows) return DIT_ERR_INVALID_ARG;
+  if (batch < 1 || batch > kMaxBatch || rows < 0 || rows > kMaxTokens || x_rows < 0 || x_row0 < 0 ||
+      (long long)x_row0 + rows > x_rows)
+    return DIT_ERR_INVALID_ARG;
   if (!adaln_supports(hidden)) return DIT_ERR_UNSUPPORTED;
   if (!aligned16(x_dev) || !aligned16(y_dev) || !aligned16(shift_lo) || !aligned16(scale_lo) ||
       !aligned16(shift_hi) || !aligned16(scale_hi) || mod_stride < 0 || mod_stride % 8 != 0 || !(eps > 0.f))
@@ -906,8 +908,10 @@ dit_status dit_adaln(int batch, int rows, int hidden, const void* x_dev, int x_r
 dit_status dit_linear(int batch, int rows, int n_out, int k, const void* a_dev, const void* w_dev, void* out_dev,
                       int ld_out, dit_epilogue epi, const void* gate_dev, long long gate_stride, void* ws,
                       size_t ws_bytes, dit_stream_t stream) {
-  if (batch < 1 || batch > kMaxBatch || rows < 1 || n_out < 1 || k < 1 || k % 8 != 0 || n_out % 32 != 0 ||
-      ld_out < n_out || ld_out % 8 != 0)
+  // rows, n_out and k up to the token limit keep every tile count and offset of the GEMM in
+  // range (tiles <= 4096 x 4096 x 64 < 2^31)
+  if (batch < 1 || batch > kMaxBatch || rows < 1 || rows > kMaxTokens || n_out < 1 || n_out > kMaxTokens || k < 1 ||
+      k > kMaxTokens || k % 8 != 0 || n_out % 32 != 0 || ld_out < n_out || ld_out % 8 != 0)
     return DIT_ERR_INVALID_ARG;
   if (!aligned16(a_dev) || !aligned16(w_dev) || !aligned16(out_dev) || !aligned16(ws)) return DIT_ERR_INVALID_ARG;
   if (ws_bytes < sizeof(DeviceStatus)) return DIT_ERR_WORKSPACE;
@@ -933,8 +937,8 @@ dit_status dit_linear(int batch, int rows, int n_out, int k, const void* a_dev, 
 
 dit_status dit_attention(int batch, int heads, int n, const void* q_dev, const void* k_dev, const void* v_dev,
                          void* out_dev, int ld_out, void* ws, size_t ws_bytes, dit_stream_t stream) {
-  if (batch < 1 || batch > kMaxBatch || heads < 1 || n < 1 || n > kMaxTokens || ld_out < 128 * heads ||
-      ld_out % 8 != 0)
+  if (batch < 1 || batch > kMaxBatch || heads < 1 || heads > kMaxTokens / 128 || n < 1 || n > kMaxTokens ||
+      ld_out < 128 * heads || ld_out % 8 != 0)
     return DIT_ERR_INVALID_ARG;
   if (!aligned16(q_dev) || !aligned16(k_dev) || !aligned16(v_dev) || !aligned16(out_dev) || !aligned16(ws))
     return DIT_ERR_INVALID_ARG;

@@ -314,7 +314,8 @@ dit_status dit_selftest_wait_timeout(void* ws, size_t ws_bytes, unsigned int lim
  * y[b, r] = (1 + scale_b) LN(x[b, x_row0 + r]) + shift_b, LN without affine, biased
  * variance, eps from the argument, statistics in fp32.  Rows r < split use
  * (shift_lo, scale_lo), the others (shift_hi, scale_hi); each vector [hidden] lives at
- * pointer + b * mod_stride elements.  x_dev [B, x_rows, hidden], y_dev [B, rows, hidden]. */
+ * pointer + b * mod_stride elements.  x_dev [B, x_rows, hidden], y_dev [B, rows, hidden].
+ * batch <= 64 and rows <= 2^20, else DIT_ERR_INVALID_ARG. */
 dit_status dit_adaln(int batch, int rows, int hidden, const void* x_dev, int x_rows, int x_row0, int split,
                      const void* shift_lo, const void* scale_lo, const void* shift_hi, const void* scale_hi,
                      long long mod_stride, float eps, void* y_dev, dit_stream_t stream);
@@ -327,7 +328,8 @@ typedef enum {
 
 /* Linear layer on the tensor cores: a_dev [B, rows, k], w_dev [n_w, k] (n_w = n_out,
  * or 2*n_out packed for SWIGLU), out_dev [B, rows, ld_out] written at columns
- * [0, n_out).  k % 8 == 0, n_out % 32 == 0 (SWIGLU: n_out % 128 == 0), ld_out % 8 == 0.
+ * [0, n_out).  k % 8 == 0, n_out % 32 == 0 (SWIGLU: n_out % 128 == 0), ld_out % 8 == 0;
+ * batch <= 64 and rows, n_out, k <= 2^20 (the token limit), else DIT_ERR_INVALID_ARG.
  * ws: any workspace of >= 256 bytes (only its status word is used). */
 dit_status dit_linear(int batch, int rows, int n_out, int k, const void* a_dev, const void* w_dev, void* out_dev,
                       int ld_out, dit_epilogue epi, const void* gate_dev, long long gate_stride, void* ws,
@@ -335,7 +337,8 @@ dit_status dit_linear(int batch, int rows, int n_out, int k, const void* a_dev, 
 
 /* Joint attention: q/k/v_dev [B, heads, n, 128] bf16 (head-major), softmax over all n
  * keys with scale 1/sqrt(128), no mask; out_dev [B, n, ld_out] with head h written at
- * columns [128h, 128h + 128).  ld_out % 8 == 0, ld_out >= 128 * heads.  ws: any
+ * columns [128h, 128h + 128).  ld_out % 8 == 0, ld_out >= 128 * heads; batch <= 64,
+ * n <= 2^20, heads <= 8192, else DIT_ERR_INVALID_ARG.  ws: any
  * workspace of >= 256 bytes (only its status word is used). */
 dit_status dit_attention(int batch, int heads, int n, const void* q_dev, const void* k_dev, const void* v_dev,
                          void* out_dev, int ld_out, void* ws, size_t ws_bytes, dit_stream_t stream);

@@ -130,9 +130,18 @@ def test_invalid_arguments_rejected_before_any_launch(dit):
     assert L.dit_linear(1, 10, 64, 60, fake, fake, fake, 64, 0, None, 0, fake, 256, None) == dit.DIT_ERR_INVALID_ARG  # k % 8
     assert L.dit_linear(1, 10, 64, 64, fake, fake, fake, 64, 1, None, 0, fake, 256, None) == dit.DIT_ERR_INVALID_ARG  # no gate
     assert L.dit_linear(1, 10, 64, 64, fake, fake, fake, 64, 0, None, 0, fake, 16, None) == dit.DIT_ERR_WORKSPACE
+    big = (1 << 20) + 32  # past the token limit: rows, n_out or k
+    assert L.dit_linear(1, big, 64, 64, fake, fake, fake, 64, 0, None, 0, fake, 256, None) == dit.DIT_ERR_INVALID_ARG
+    assert L.dit_linear(1, 10, big, 64, fake, fake, fake, big, 0, None, 0, fake, 256, None) == dit.DIT_ERR_INVALID_ARG
+    assert L.dit_linear(1, 10, 64, big, fake, fake, fake, 64, 0, None, 0, fake, 256, None) == dit.DIT_ERR_INVALID_ARG
+    assert L.dit_linear(65, 10, 64, 64, fake, fake, fake, 64, 0, None, 0, fake, 256, None) == dit.DIT_ERR_INVALID_ARG
     assert L.dit_attention(1, 2, 10, fake, fake, fake, fake, 200, fake, 256, None) == dit.DIT_ERR_INVALID_ARG  # ld < 256
+    assert L.dit_attention(1, 1 << 24, 10, fake, fake, fake, fake, 256, fake, 256, None) == dit.DIT_ERR_INVALID_ARG
+    assert L.dit_attention(1, 2, big, fake, fake, fake, fake, 256, fake, 256, None) == dit.DIT_ERR_INVALID_ARG
     assert L.dit_adaln(1, 4, 300, fake, 4, 0, 0, fake, fake, fake, fake, 0, 1e-6, fake, None) == dit.DIT_ERR_UNSUPPORTED
     assert L.dit_adaln(1, 4, 256, fake, 3, 0, 0, fake, fake, fake, fake, 0, 1e-6, fake, None) == dit.DIT_ERR_INVALID_ARG
+    assert L.dit_adaln(1, big, 256, fake, big, 0, 0, fake, fake, fake, fake, 0, 1e-6, fake, None) == dit.DIT_ERR_INVALID_ARG
+    assert L.dit_adaln(65, 4, 256, fake, 4, 0, 0, fake, fake, fake, fake, 0, 1e-6, fake, None) == dit.DIT_ERR_INVALID_ARG
     assert L.dit_timing_begin(0) == dit.DIT_ERR_INVALID_ARG
     assert dit.dit_launch_count() == before
 

@@ -125,6 +125,21 @@ def test_linear_store(dit, batch, rows, n, k, ws):
     assert (out[..., n:] == 7.0).all()  # columns past n_out untouched
 
 
+def test_linear_at_the_row_limit(dit, ws):
+    """The GEMM at the library's token limit (2^20 rows less a ragged 13), two batches, a
+    ragged n (96) and k (72): 16384 row tiles.  Sampled rows of both batches (first tiles,
+    the middle, the last full tile, the ragged tail) against the product in fp64."""
+    batch, rows, n, k = 2, (1 << 20) - 13, 96, 72
+    a = _randn((batch, rows, k), 1.0, seed=41)
+    w = _randn((n, k), 0.05, seed=42)
+    out = torch.zeros((batch, rows, n), dtype=torch.bfloat16, device=DEV)
+    dit.dit_linear(batch, rows, n, k, a.to(DEV), w.to(DEV), out, n, dit.DIT_EPI_STORE, None, 0, ws, ws.numel())
+    _check_status(dit, ws)
+    sel = [0, 1, 127, 128, 255, 256, rows // 2, rows // 2 + 129, rows - 300, rows - 129, rows - 13, rows - 1]
+    want = Hx.to_np(a[:, sel]) @ Hx.to_np(w).T
+    _cmp(out[:, sel], want, atol=1e-2 * np.abs(want).max())
+
+
 @pytest.mark.parametrize("batch,rows,n,k", [(1, 256, 256, 256), (2, 300, 3072, 320)])
 def test_linear_gated_residual(dit, batch, rows, n, k, ws):
     a = _randn((batch, rows, k), 1.0, seed=5).to(DEV)
