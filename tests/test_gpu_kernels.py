@@ -86,6 +86,30 @@ def test_adaln(dit, hidden, rows, split, batch):
     _cmp(y, want)
 
 
+def test_adaln_at_the_row_limit(dit):
+    """adaLN at the library's token limit (2^20 rows less a ragged 13) for two batch rows,
+    hidden 256, with the split between the two modulation pairs in the middle: ~2 x 2^20
+    rows streamed through each CTA's ring.  Sampled rows on both sides of the split, at
+    the start and the end, against the oracle."""
+    batch, rows, hidden = 2, (1 << 20) - 13, 256
+    split = rows // 2 + 7
+    x = _randn((batch, rows, hidden), 1.5, seed=51, mean=0.3)
+    mod = _randn((batch, 4, hidden), 0.1, seed=52)
+    y = torch.empty((batch, rows, hidden), dtype=torch.bfloat16, device=DEV)
+    md = mod.to(DEV)
+    dit.dit_adaln(batch, rows, hidden, x.to(DEV), rows, 0, split, md[:, 0], md[:, 1], md[:, 2], md[:, 3],
+                  4 * hidden, 1e-6, y)
+    torch.cuda.synchronize()
+    sel = [0, 1, 31, 32, split - 1, split, split + 1, rows - 300, rows - 13, rows - 1]
+    xn, mn = Hx.to_np(x[:, sel]), Hx.to_np(mod)
+    want = np.empty((batch, len(sel), hidden))
+    for b in range(batch):
+        for i, r in enumerate(sel):
+            lo = r < split
+            want[b, i] = O.adaln(xn[b, i:i + 1], mn[b, 0 if lo else 2], mn[b, 1 if lo else 3], 1e-6)[0]
+    _cmp(y[:, sel], want)
+
+
 WIDE_MOD = synth.Widths(hidden=4096, heads=32, head_dim=128, mlp_hidden=12288, n_dual=1, n_single=1)
 
 
