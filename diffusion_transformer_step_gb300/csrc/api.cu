@@ -148,11 +148,14 @@ inline bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<
 
 dit_status check_config(const dit_config* c) {
   if (!c) return DIT_ERR_INVALID_ARG;
-  if (c->head_dim != 128 || c->heads <= 0 || c->hidden != c->heads * 128) return DIT_ERR_UNSUPPORTED;
+  // hidden first (at most 4096), so that heads * 128 below cannot overflow; the GEMM widths
+  // stay within dit_linear's limits
   if (!adaln_supports(c->hidden)) return DIT_ERR_UNSUPPORTED;
-  if (c->mlp_hidden <= 0 || c->mlp_hidden % 128 != 0) return DIT_ERR_UNSUPPORTED;
-  if (c->in_channels <= 0 || c->in_channels % 32 != 0) return DIT_ERR_UNSUPPORTED;
-  if (c->txt_dim <= 0 || c->txt_dim % 8 != 0) return DIT_ERR_UNSUPPORTED;
+  if (c->head_dim != 128 || c->heads <= 0 || c->heads > c->hidden || c->hidden != c->heads * 128)
+    return DIT_ERR_UNSUPPORTED;
+  if (c->mlp_hidden <= 0 || c->mlp_hidden % 128 != 0 || c->mlp_hidden > kMaxTokens / 2) return DIT_ERR_UNSUPPORTED;
+  if (c->in_channels <= 0 || c->in_channels % 32 != 0 || c->in_channels > kMaxTokens) return DIT_ERR_UNSUPPORTED;
+  if (c->txt_dim <= 0 || c->txt_dim % 8 != 0 || c->txt_dim > kMaxTokens) return DIT_ERR_UNSUPPORTED;
   if (c->n_dual < 0 || c->n_single < 0) return DIT_ERR_INVALID_ARG;
   int sum = 0;
   for (int i = 0; i < 4; ++i) {
@@ -628,6 +631,7 @@ dit_status dit_token_ids(const dit_shape* shape, int grid_h, int grid_w, const i
   for (int i = 0; i < n_refs; ++i) {
     if (ref_grids_host[2 * i] < 1 || ref_grids_host[2 * i + 1] < 1) return DIT_ERR_INVALID_ARG;
     nref += (long long)ref_grids_host[2 * i] * ref_grids_host[2 * i + 1];
+    if (nref > shape->n_ref) return DIT_ERR_INVALID_ARG;  // also keeps the sum far from overflow
   }
   if (nref != shape->n_ref) return DIT_ERR_INVALID_ARG;
   int32_t* o = ids_host;
@@ -658,7 +662,9 @@ dit_status dit_rope_table(const dit_config* cfg, const int32_t* ids_dev, int n, 
 
 dit_status dit_pack_mlp_in(const void* src_dev, void* dst_dev, int mlp_hidden, int cols, dit_stream_t stream) {
   if (!aligned16(src_dev) || !aligned16(dst_dev)) return DIT_ERR_INVALID_ARG;
-  if (mlp_hidden <= 0 || mlp_hidden % 128 != 0 || cols <= 0 || cols % 8 != 0) return DIT_ERR_INVALID_ARG;
+  if (mlp_hidden <= 0 || mlp_hidden % 128 != 0 || mlp_hidden > kMaxTokens / 2 || cols <= 0 || cols % 8 != 0 ||
+      cols > kMaxTokens)
+    return DIT_ERR_INVALID_ARG;
   const uintptr_t a = (uintptr_t)src_dev, b = (uintptr_t)dst_dev, len = (uintptr_t)2 * mlp_hidden * cols * 2;
   if (a < b + len && b < a + len) return DIT_ERR_INVALID_ARG;
   return cuda_status(launch_pack_mlp_in((const bf16*)src_dev, (bf16*)dst_dev, mlp_hidden, cols, (cudaStream_t)stream));
@@ -666,7 +672,8 @@ dit_status dit_pack_mlp_in(const void* src_dev, void* dst_dev, int mlp_hidden, i
 
 dit_status dit_quantize_rows_fp8(const void* w_dev, int rows, int cols, void* q_dev, float* scale_dev,
                                  dit_stream_t stream) {
-  if (!aligned16(w_dev) || !aligned16(q_dev) || !aligned16(scale_dev) || rows < 1 || cols < 16 || cols % 16 != 0)
+  if (!aligned16(w_dev) || !aligned16(q_dev) || !aligned16(scale_dev) || rows < 1 || rows > kMaxTokens || cols < 16 ||
+      cols % 16 != 0 || cols > kMaxTokens)
     return DIT_ERR_INVALID_ARG;
   return cuda_status(launch_quantize_rows((const bf16*)w_dev, rows, cols, (uint8_t*)q_dev, scale_dev,
                                           (cudaStream_t)stream));

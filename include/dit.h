@@ -60,9 +60,10 @@ typedef enum {
   DIT_ERR_TIMEOUT = 5
 } dit_status;
 
-/* Model widths.  Supported: head_dim == 128, hidden == heads * 128, hidden % 256 == 0,
- * hidden <= 8192, mlp_hidden % 128 == 0, in_channels % 32 == 0, txt_dim % 8 == 0,
- * axes_dim[i] even with sum == head_dim, rope_theta > 0, eps > 0.
+/* Model widths.  Supported: head_dim == 128, hidden == heads * 128 with hidden / 256 in
+ * {1, 2, 3, 4, 5, 6, 8, 10, 12, 14, 16} (hidden <= 4096), mlp_hidden % 128 == 0 and
+ * <= 2^19, in_channels % 32 == 0 and <= 2^20, txt_dim % 8 == 0 and <= 2^20, axes_dim[i]
+ * even with sum == head_dim, rope_theta > 0, eps > 0.
  * klein 4B: {3072, 24, 128, 9216, 5, 20, 128, 7680, 2000.f, {32,32,32,32}, 1e-6f}. */
 typedef struct {
   int hidden, heads, head_dim, mlp_hidden, n_dual, n_single, in_channels, txt_dim;
@@ -187,14 +188,16 @@ dit_status dit_rope_table(const dit_config* cfg, const int32_t* ids_dev, int n, 
 /* Weight preparation: rearrange an MLP-in weight from the logical order [gate (F rows);
  * up (F rows)] into the packed order the library reads: blocks of 256 rows, block j =
  * [gate rows 128j .. 128j+127 ; up rows 128j .. 128j+127].  src_dev and dst_dev are
- * [2F, cols] bf16 device buffers that must not overlap.  For a single-stream qkv_mlp
+ * [2F, cols] bf16 device buffers that must not overlap; F % 128 == 0, F <= 2^19,
+ * cols % 8 == 0, cols <= 2^20.  For a single-stream qkv_mlp
  * weight, pack its last 2F rows (pointer offset 3H * cols elements) and copy the first
  * 3H rows unchanged. */
 dit_status dit_pack_mlp_in(const void* src_dev, void* dst_dev, int mlp_hidden, int cols, dit_stream_t stream);
 
 /* Weight preparation for the e4m3 path: for each row r of w_dev [rows, cols] (bf16),
  * scale_dev[r] = max|w[r, :]| / 448 and q_dev[r, c] = e4m3(w[r, c] / scale[r]) (round to
- * nearest, saturating).  q_dev [rows, cols] bytes, scale_dev [rows] fp32; cols % 16 == 0. */
+ * nearest, saturating).  q_dev [rows, cols] bytes, scale_dev [rows] fp32; cols % 16 == 0,
+ * rows and cols <= 2^20. */
 dit_status dit_quantize_rows_fp8(const void* w_dev, int rows, int cols, void* q_dev, float* scale_dev,
                                  dit_stream_t stream);
 

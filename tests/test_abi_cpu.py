@@ -63,6 +63,12 @@ def test_token_ids_rejects_inconsistent_grid(dit):
     with pytest.raises(dit.DitError) as e:
         dit.dit_token_ids(shape, 3, 3)
     assert e.value.status == dit.DIT_ERR_INVALID_ARG
+    # reference grids whose token counts overflow any sum, or exceed n_ref on the way
+    shape = dit.make_shape(1, 4, 9, 6)
+    for refs in (((2, 3), (1 << 30, 1 << 30)), ((1 << 30, 1 << 30), (1 << 30, 1 << 30)), ((4, 4),)):
+        with pytest.raises(dit.DitError) as e:
+            dit.dit_token_ids(shape, 3, 3, refs)
+        assert e.value.status == dit.DIT_ERR_INVALID_ARG
 
 
 def test_workspace_size_grows_with_shape(dit):
@@ -93,8 +99,10 @@ def test_workspace_size_at_the_largest_accepted_shape_does_not_wrap(dit):
 
 def test_unsupported_configs_rejected(dit):
     shape = dit.make_shape(1, 8, 16, 0)
+    big = (1 << 20) + 128  # past the GEMM width limit
     for field, val in (("head_dim", 64), ("hidden", 3000), ("mlp_hidden", 100), ("in_channels", 20),
-                       ("txt_dim", 7)):
+                       ("txt_dim", 7), ("heads", 1 << 25), ("heads", 23), ("mlp_hidden", big),
+                       ("in_channels", big), ("txt_dim", big)):
         c = dit.dit_config_klein()
         setattr(c, field, val)
         n = C.c_size_t(0)
@@ -126,6 +134,7 @@ def test_invalid_arguments_rejected_before_any_launch(dit):
     assert L.dit_rope_table(C.byref(c), fake + 4, 10, fake, None) == dit.DIT_ERR_INVALID_ARG
     assert L.dit_pack_mlp_in(fake, fake + 16, 9216, 3072, None) == dit.DIT_ERR_INVALID_ARG   # overlap
     assert L.dit_pack_mlp_in(fake, fake, 100, 3072, None) == dit.DIT_ERR_INVALID_ARG
+    assert L.dit_pack_mlp_in(fake, fake + (1 << 40), 1 << 30, 64, None) == dit.DIT_ERR_INVALID_ARG  # 2F past limit
     assert L.dit_linear(1, 10, 48, 64, fake, fake, fake, 48, 0, None, 0, fake, 256, None) == dit.DIT_ERR_INVALID_ARG  # n % 32
     assert L.dit_linear(1, 10, 64, 60, fake, fake, fake, 64, 0, None, 0, fake, 256, None) == dit.DIT_ERR_INVALID_ARG  # k % 8
     assert L.dit_linear(1, 10, 64, 64, fake, fake, fake, 64, 1, None, 0, fake, 256, None) == dit.DIT_ERR_INVALID_ARG  # no gate
@@ -242,6 +251,8 @@ def test_loop_host_graph_and_helper_calls_validate_before_any_cuda_call(dit):
     assert L.dit_quantize_rows_fp8(fake, 4, 24, fake, fake, None) == INV       # cols % 16
     assert L.dit_quantize_rows_fp8(fake, 4, 32, fake, fake + 4, None) == INV   # misaligned scales
     assert L.dit_quantize_rows_fp8(fake, 0, 32, fake, fake, None) == INV
+    assert L.dit_quantize_rows_fp8(fake, (1 << 20) + 1, 32, fake, fake, None) == INV
+    assert L.dit_quantize_rows_fp8(fake, 4, (1 << 20) + 16, fake, fake, None) == INV
     assert L.dit_selftest_wait_timeout(fake, 256, 0, None) == INV
     assert L.dit_selftest_wait_timeout(fake, 256, 2000000, None) == INV
     assert L.dit_selftest_wait_timeout(fake, 8, 100, None) == INV
