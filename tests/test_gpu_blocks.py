@@ -210,6 +210,29 @@ def test_step_tiny_e4m3(dit, wl):
     assert cs8 >= bar8
 
 
+TINY_MIN = synth.Workload("tiny_min", synth.TINY, 1, 1, (1, 1))                      # N = 2
+TINY_MIN_REF = synth.Workload("tiny_min_ref_b2", synth.TINY, 2, 1, (1, 1), ((1, 1),))  # N = 3
+
+
+@pytest.mark.parametrize("wl", [TINY_MIN, TINY_MIN_REF], ids=lambda w: w.name)
+def test_step_at_the_smallest_shapes(dit, wl):
+    """One text row and one image token (and one reference token): every GEMM problem is a
+    single row in a 256-row tile, attention a single partial key block of two or three
+    keys.  The step in bf16 and in e4m3 against the oracle's (fp64), at the step bars."""
+    logical = _tiny_step_weights(wl, seed=9)
+    inp = synth.step_inputs(wl, seed=9)
+    vel, _ = _step(dit, wl, logical, inp)
+    want = _oracle_step(wl, logical, inp, np.float64, range(wl.batch))
+    cs = Hx.cosine(Hx.to_np(vel), want)
+    vel8, _ = _step(dit, wl, logical, inp, dit.DeviceWeights(wl.widths, logical, fp8=True))
+    want8 = _oracle_step(wl, logical, inp, np.float64, range(wl.batch), e4m3="all")
+    bar8 = STEP_COS - 2.0 * (1.0 - Hx.cosine(want8, want))
+    cs8 = Hx.cosine(Hx.to_np(vel8), want8)
+    print(f"step {wl.name}: cos {cs:.6f}; e4m3 cos {cs8:.6f} (bar {bar8:.6f})")
+    assert cs >= STEP_COS and cs8 >= bar8
+    assert not torch.equal(vel, vel8)
+
+
 def test_step_at_the_largest_batch(dit):
     """Batch 64, the largest the library accepts, each row with its own sigma (the
     modulation runs as eight launches of eight rows; the attention grid's z extent is 64):
