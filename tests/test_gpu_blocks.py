@@ -403,6 +403,33 @@ def test_denoise_loop_tiny(dit, wl):
     assert cs >= 0.999 and dcs >= STEP_COS
 
 
+def test_denoise_loop_at_the_step_limit(dit):
+    """Eight Euler steps, the most the loop accepts, at batch 2 (TINY_REF): the modulation
+    of all 16 (step, row) pairs takes two weight passes of eight rows.  Against the oracle's
+    loop over the same eight-step schedule (reading R19 with 8 in place of 4)."""
+    wl = TINY_REF
+    logical = _tiny_step_weights(wl, seed=10)
+    inp = synth.step_inputs(wl, seed=10)
+    sig = O.sigma_schedule(float(inp["sigma"][0]), 8).astype(np.float32)
+    W = dit.DeviceWeights(wl.widths, logical)
+    shape, rope, ws, nbytes = _setup(dit, wl, W)
+    x = inp["img_tokens"].to(DEV).clone()
+    dit.dit_denoise_fwd(W.w, shape, x, inp["ref_tokens"].to(DEV), inp["txt_emb"].to(DEV), rope, sig.tolist(), ws,
+                        nbytes)
+    _status(dit, ws)
+    ow = Hx.oracle_weights(wl.widths, logical)
+    ids = O.token_ids(wl.n_txt, *wl.grid, wl.ref_grids)
+    x0 = Hx.to_np(inp["img_tokens"])
+    want = O.denoise(ow, x0, Hx.to_np(inp["ref_tokens"]), Hx.to_np(inp["txt_emb"]), ids, sig.astype(np.float64))
+    got = Hx.to_np(x)
+    cs, dcs = Hx.cosine(got, want), Hx.cosine(got - x0, want - x0)
+    print(f"denoise 8 steps {wl.name}: cos {cs:.7f} displacement-cos {dcs:.6f}")
+    assert cs >= 0.999 and dcs >= STEP_COS
+    with pytest.raises(dit.DitError):  # nine steps are refused
+        dit.dit_denoise_fwd(W.w, shape, x, inp["ref_tokens"].to(DEV), inp["txt_emb"].to(DEV), rope,
+                            O.sigma_schedule(0.9, 9).tolist(), ws, nbytes)
+
+
 @pytest.mark.parametrize("wl", [synth.WORKLOADS["tiny"], TINY_REF], ids=lambda w: w.name)
 def test_denoise_loop_tiny_e4m3(dit, wl):
     """The 4-step loop with every block projection in e4m3 against the oracle's e4m3 loop
