@@ -86,6 +86,27 @@ def test_adaln(dit, hidden, rows, split, batch):
     _cmp(y, want)
 
 
+@pytest.mark.parametrize("axes,theta", [((16, 56, 56, 0), 10000.0), ((0, 64, 32, 32), 2000.0)])
+def test_rope_table_other_axis_splits(dit, axes, theta):
+    """The table for other splits of the 128 head dims over the four axes (one of them empty)
+    and another theta: every pair's cos / sin against the oracle's table of that split."""
+    n_txt, grid, refs = 16, (6, 10), ((3, 4),)
+    shape = dit.make_shape(1, n_txt, grid[0] * grid[1], 12)
+    ids = dit.dit_token_ids(shape, grid[0], grid[1], refs)
+    N = ids.shape[0]
+    cfg = dit.dit_config_klein()
+    for i, d in enumerate(axes):
+        cfg.axes_dim[i] = d
+    cfg.rope_theta = theta
+    table = torch.empty((N, 64, 2), dtype=torch.float32, device=DEV)
+    dit.dit_rope_table(cfg, ids.to(DEV), N, table)
+    torch.cuda.synchronize()
+    c, s = O.rope_table(O.token_ids(n_txt, grid[0], grid[1], refs), axes, theta)
+    t = table.cpu().numpy().astype(np.float64)
+    np.testing.assert_allclose(t[..., 0], c, rtol=0, atol=1.2e-7)
+    np.testing.assert_allclose(t[..., 1], s, rtol=0, atol=1.2e-7)
+
+
 def test_adaln_at_the_row_limit(dit):
     """adaLN at the library's token limit (2^20 rows less a ragged 13) for two batch rows,
     hidden 256, with the split between the two modulation pairs in the middle: ~2 x 2^20
