@@ -66,9 +66,11 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) adaln_kernel(AdaLNArgs a) {
   uint8_t* buf0 = smem_raw + (size_t)(warp * 2) * kRowBytes;
   uint8_t* buf1 = buf0 + kRowBytes;
   uint64_t* bar = bars[warp];
-  const long long total = (long long)a.batch * a.rows;
-  const long long stride = (long long)gridDim.x * nwarps;
-  long long r = (long long)blockIdx.x * nwarps + warp;
+  // Row indices in 32 bits (batch * rows <= 64 * 2^20 by the entry points' limits): the
+  // per-row batch / row split is then a 32-bit division, not a 64-bit library routine.
+  const int total = a.batch * a.rows;
+  const int stride = (int)gridDim.x * nwarps;
+  int r = (int)blockIdx.x * nwarps + warp;
 
   if (lane == 0) {
     mbar_init(&bar[0], 1);
@@ -81,16 +83,16 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) adaln_kernel(AdaLNArgs a) {
   grid_dependency_wait();  // x and y belong to earlier kernels of the stream
   allow_dependents();
 
-  auto row_src = [&](long long row) -> const uint8_t* {
-    const int b = (int)(row / a.rows);
-    const int rr = (int)(row - (long long)b * a.rows);
+  auto row_src = [&](int row) -> const uint8_t* {
+    const int b = row / a.rows;
+    const int rr = row - b * a.rows;
     return reinterpret_cast<const uint8_t*>(a.x) +
            (b * a.x_bstride + (long long)(a.x_row0 + rr) * H) * (F32IN ? 4 : 2);
   };
-  long long issued = 0;  // rows copied in by this warp (lane 0's count)
+  int issued = 0;  // rows copied in by this warp (lane 0's count)
   if (lane == 0) {
     for (int st = 0; st < 2; ++st) {
-      const long long row = r + st * stride;
+      const int row = r + st * stride;
       if (row < total) {
         mbar_arrive_expect_tx(&bar[st], kRowBytes);
         bulk_copy_g2s(st ? buf1 : buf0, row_src(row), kRowBytes, &bar[st]);
@@ -99,15 +101,15 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) adaln_kernel(AdaLNArgs a) {
     }
   }
 
-  long long consumed = 0;
+  int consumed = 0;
   for (int i = 0; r < total; ++i, r += stride) {
     const int st = i & 1;
     bool ok = mbar_wait_sleep(&bar[st], (uint32_t)(i >> 1) & 1u, wc, kSiteAdaLN);
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) break;
     const uint8_t* buf = st ? buf1 : buf0;
-    const int b = (int)(r / a.rows);
-    const int rw = (int)(r - (long long)b * a.rows);
+    const int b = r / a.rows;
+    const int rw = r - b * a.rows;
 
     // pass 1: shifted sums
     const float shift0 = F32IN ? reinterpret_cast<const float*>(buf)[0]
@@ -203,7 +205,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) adaln_kernel(AdaLNArgs a) {
     __syncwarp();
     if (lane == 0) {
       fence_proxy_async_smem();
-      const long long nrow = r + 2 * stride;
+      const int nrow = r + 2 * stride;
       if (nrow < total) {
         mbar_arrive_expect_tx(&bar[st], kRowBytes);
         bulk_copy_g2s(st ? buf1 : buf0, row_src(nrow), kRowBytes, &bar[st]);
@@ -215,7 +217,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) adaln_kernel(AdaLNArgs a) {
   // block's shared memory is released.
   if (lane == 0) {
     const uint64_t t0 = global_timer_ns();
-    for (long long k = consumed; k < issued; ++k)
+    for (int k = consumed; k < issued; ++k)
       while (!mbar_try(&bar[k & 1], (uint32_t)(k >> 1) & 1u) && global_timer_ns() - t0 < 100000000ull) {
       }
   }
@@ -351,6 +353,7 @@ bool adaln_supports(int hidden) {
 
 cudaError_t launch_adaln(const AdaLNArgs& a, cudaStream_t s) {
   if ((long long)a.batch * a.rows == 0) return cudaSuccess;
+  if ((long long)a.batch * a.rows > (1ll << 26)) return cudaErrorInvalidValue;  // the kernel's 32-bit row index
   switch (a.hidden / 256) {
     case 1: return launch_vpl<1>(a, s);
     case 2: return launch_vpl<2>(a, s);
