@@ -519,6 +519,13 @@ def test_blocks_wider_config(dit, kind):
     run_block(dit, kind, WIDE_WL, seed=4)
 
 
+@pytest.mark.parametrize("kind", ["dual", "single"])
+def test_blocks_wider_config_fp8(dit, kind):
+    """The e4m3 blocks at hidden 4096: the single-stream out-projection's quantising pass
+    then takes rows of H + F = 16 384 columns, the longest it accepts."""
+    run_block(dit, kind, WIDE_WL, seed=4, fp8="all")
+
+
 @pytest.mark.parametrize("wl,scope", [(synth.WORKLOADS["single_block_1024"], "all"), (TINY_REF, "all"),
                                       (TINY_REF, "fused")], ids=lambda v: getattr(v, "name", v))
 def test_single_block_fp8(dit, wl, scope):
