@@ -326,7 +326,9 @@ cudaError_t launch_kind(const AdaLNArgs& a, cudaStream_t s) {
   const long long cap = (long long)sm_count();
   if (grid > cap) grid = cap;
   auto k = adaln_kernel<VPL, F32IN, kFp8Out>;
-  if (smem > 48 * 1024) {
+  // The static shared memory (row barriers and the abort flag, under 1 KB) counts against
+  // the same 48 KB default as the dynamic part: hidden 768 asks for exactly 48 KB dynamic.
+  if (smem + 1024 > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }

@@ -519,6 +519,17 @@ def test_blocks_wider_config(dit, kind):
     run_block(dit, kind, WIDE_WL, seed=4)
 
 
+# A narrower width than klein's whose adaLN asks for exactly 48 KB of dynamic shared memory
+# (hidden 768: 16 warps x 2 staged rows of 1.5 KB), the edge of the default per-block limit.
+NARROW = synth.Widths(hidden=768, heads=6, head_dim=128, mlp_hidden=2304, n_dual=1, n_single=1)
+NARROW_WL = synth.Workload("narrow_768", NARROW, 2, 40, (6, 10), ((3, 4),))
+
+
+@pytest.mark.parametrize("kind", ["dual", "single"])
+def test_blocks_narrow_config(dit, kind):
+    run_block(dit, kind, NARROW_WL, seed=6)
+
+
 @pytest.mark.parametrize("kind", ["dual", "single"])
 def test_blocks_wider_config_fp8(dit, kind):
     """The e4m3 blocks at hidden 4096: the single-stream out-projection's quantising pass

@@ -107,6 +107,25 @@ def test_rope_table_other_axis_splits(dit, axes, theta):
     np.testing.assert_allclose(t[..., 1], s, rtol=0, atol=1.2e-7)
 
 
+@pytest.mark.parametrize("hidden", [256 * v for v in (1, 2, 3, 4, 5, 6, 8, 10, 12, 14, 16)])
+def test_adaln_every_supported_width(dit, hidden):
+    """Every hidden width the kernel is instantiated for (hidden / 256 vectors of 8 per lane),
+    two batch rows, a ragged row count and a split, every element against the oracle."""
+    batch, rows, split = 2, 37, 11
+    x = _randn((batch, rows, hidden), 1.5, seed=61, mean=-0.4).to(DEV)
+    mod = _randn((batch, 4, hidden), 0.1, seed=62).to(DEV)
+    y = torch.empty((batch, rows, hidden), dtype=torch.bfloat16, device=DEV)
+    dit.dit_adaln(batch, rows, hidden, x, rows, 0, split, mod[:, 0], mod[:, 1], mod[:, 2], mod[:, 3], 4 * hidden,
+                  1e-6, y)
+    torch.cuda.synchronize()
+    xn, mn = Hx.to_np(x), Hx.to_np(mod)
+    want = np.empty((batch, rows, hidden))
+    for b in range(batch):
+        want[b, :split] = O.adaln(xn[b, :split], mn[b, 0], mn[b, 1], 1e-6)
+        want[b, split:] = O.adaln(xn[b, split:], mn[b, 2], mn[b, 3], 1e-6)
+    _cmp(y, want)
+
+
 def test_adaln_at_the_row_limit(dit):
     """adaLN at the library's token limit (2^20 rows less a ragged 13) for two batch rows,
     hidden 256, with the split between the two modulation pairs in the middle: ~2 x 2^20
