@@ -233,6 +233,32 @@ def test_step_at_the_smallest_shapes(dit, wl):
     assert not torch.equal(vel, vel8)
 
 
+# Input and text widths below one 64-deep k-block (in_channels 32, text features 40), a
+# final projection 32 wide, an MLP width that is an odd multiple of 128, three blocks.
+ODD_IO = synth.Widths(hidden=512, heads=4, head_dim=128, mlp_hidden=1280, n_dual=1, n_single=2, in_channels=32,
+                      txt_dim=40)
+ODD_IO_WL = synth.Workload("odd_io", ODD_IO, 2, 20, (5, 7), ((2, 3),))
+
+
+def test_step_other_io_widths(dit):
+    """The step with in_channels 32 and 40-wide text features (the embedders' GEMMs then
+    have K below one k-block) and a 32-wide final projection, bf16 and e4m3, against the
+    oracle's."""
+    wl = ODD_IO_WL
+    logical = _tiny_step_weights(wl, seed=12)
+    inp = synth.step_inputs(wl, seed=12)
+    vel, _ = _step(dit, wl, logical, inp)
+    want = _oracle_step(wl, logical, inp, np.float64, range(wl.batch))
+    cs = Hx.cosine(Hx.to_np(vel), want)
+    vel8, _ = _step(dit, wl, logical, inp, dit.DeviceWeights(wl.widths, logical, fp8=True))
+    want8 = _oracle_step(wl, logical, inp, np.float64, range(wl.batch), e4m3="all")
+    bar8 = STEP_COS - 2.0 * (1.0 - Hx.cosine(want8, want))
+    cs8 = Hx.cosine(Hx.to_np(vel8), want8)
+    print(f"step {wl.name}: cos {cs:.6f}; e4m3 cos {cs8:.6f} (bar {bar8:.6f})")
+    assert vel.shape == (2, 35, 32)
+    assert cs >= STEP_COS and cs8 >= bar8
+
+
 def test_step_at_the_largest_batch(dit):
     """Batch 64, the largest the library accepts, each row with its own sigma (the
     modulation runs as eight launches of eight rows; the attention grid's z extent is 64):

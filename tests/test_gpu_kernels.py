@@ -175,7 +175,7 @@ def test_modulation(dit, wd, batch, ws):
 
 
 @pytest.mark.parametrize("batch,rows,n,k", [(1, 128, 256, 64), (2, 300, 288, 320), (1, 1000, 768, 3072),
-                                            (3, 17, 128, 7680)])
+                                            (3, 17, 128, 7680), (1, 70, 32, 8), (2, 130, 64, 40)])
 def test_linear_store(dit, batch, rows, n, k, ws):
     a = _randn((batch, rows, k), 1.0, seed=3).to(DEV)
     w = _randn((n, k), 0.05, seed=4).to(DEV)
