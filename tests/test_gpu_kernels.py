@@ -153,8 +153,15 @@ def test_adaln_at_the_row_limit(dit):
 WIDE_MOD = synth.Widths(hidden=4096, heads=32, head_dim=128, mlp_hidden=12288, n_dual=1, n_single=1)
 
 
+# hidden 768 and 1536: eight batch rows of a 1536-wide input fill exactly the default 48 KB
+# of dynamic shared memory of the GEMV
+MOD_768 = synth.Widths(hidden=768, heads=6, head_dim=128, mlp_hidden=2304, n_dual=1, n_single=1)
+MOD_1536 = synth.Widths(hidden=1536, heads=12, head_dim=128, mlp_hidden=4608, n_dual=1, n_single=1)
+
+
 @pytest.mark.parametrize("wd,batch", [(synth.TINY, 1), (synth.TINY, 3), (synth.KLEIN, 1), (synth.KLEIN, 3),
-                                      (synth.KLEIN, 11), (WIDE_MOD, 8)],
+                                      (synth.KLEIN, 11), (WIDE_MOD, 8), (MOD_768, 8), (MOD_1536, 8),
+                                      (MOD_1536, 5)],
                          ids=lambda v: getattr(v, "hidden", v))
 def test_modulation(dit, wd, batch, ws):
     """Every element of the modulation vector against the oracle; batch 11 runs as launches
