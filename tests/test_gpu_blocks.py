@@ -234,8 +234,9 @@ def test_step_at_the_smallest_shapes(dit, wl):
 
 
 # Input and text widths below one 64-deep k-block (in_channels 32, text features 40), a
-# final projection 32 wide, an MLP width that is an odd multiple of 128, three blocks.
-ODD_IO = synth.Widths(hidden=512, heads=4, head_dim=128, mlp_hidden=1280, n_dual=1, n_single=2, in_channels=32,
+# final projection 32 wide, an MLP width that is an odd multiple of 128 (1152: SwiGLU tiles
+# of 128 gate + 128 up rows, 9 of them), three blocks.
+ODD_IO = synth.Widths(hidden=512, heads=4, head_dim=128, mlp_hidden=1152, n_dual=1, n_single=2, in_channels=32,
                       txt_dim=40)
 ODD_IO_WL = synth.Workload("odd_io", ODD_IO, 2, 20, (5, 7), ((2, 3),))
 
