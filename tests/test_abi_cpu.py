@@ -259,3 +259,22 @@ def test_loop_host_graph_and_helper_calls_validate_before_any_cuda_call(dit):
     assert L.dit_sync_status(None, None, None) == INV
     assert L.dit_sync_status(fake + 8, None, None) == INV
     assert dit.dit_launch_count() == before
+
+
+def test_header_is_plain_c_and_host_entry_points_work_from_c(dit, tmp_path):
+    """tests/c/abi_from_c.c, compiled as C11 with warnings as errors against include/dit.h
+    and linked to libdit.so: the header needs no C++ or CUDA header, and the host-side
+    calls (klein config, workspace sizes, token ids, refusals before any launch) behave
+    as documented when called from C."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    pkg = os.path.dirname(dit.LIB_PATH)
+    exe = str(tmp_path / "abi_from_c")
+    subprocess.run([gcc, "-std=c11", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"),
+                    os.path.join(ROOT, "tests", "c", "abi_from_c.c"), "-L", pkg, "-ldit", f"-Wl,-rpath,{pkg}",
+                    "-o", exe], check=True)
+    out = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert out.returncode == 0 and out.stdout.strip() == "ok", out.stdout + out.stderr
